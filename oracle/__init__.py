@@ -1,0 +1,102 @@
+"""CPU oracle for deterministic exact ragged top-k (TEST INFRASTRUCTURE ONLY).
+
+Only the tests, ``__graft_entry__.smoke()`` and the benchmark's CPU-baseline /
+reference arm may import this package.  The product path (the CUDA library and
+its Python binding) never touches it, and the oracle shares no code with that
+path: ``oracle.c`` is compiled on its own with the host C compiler.
+
+Every function pins to the definition in sglang PR #31115 "Add opt-in
+deterministic CuTe-DSL DSA top-k backend" (PR summary, hardening commit,
+Modifications): canonical order score desc / index asc on bitwise-equal
+scores under the bitwise total order of fp32 patterns, front-packed output,
+-1 padding.  The pinning tests live in ``tests/test_oracle.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD_DIR = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
+_lock = threading.Lock()
+_lib = None
+
+FLAG_LEN_ENVELOPE = 1
+FLAG_BAD_WINDOW = 2
+PAD_VALUE_BITS = 0xFF800000
+
+
+def build(force: bool = False) -> str:
+    """Compile oracle.c into a shared library beside it (host C compiler)."""
+    os.makedirs(_BUILD_DIR, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-Wall", "-Wextra", "-shared", "-fPIC",
+           "-pthread", _SRC, "-o", tmp]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            lib.oracle_order_key.argtypes = [ctypes.c_uint32]
+            lib.oracle_order_key.restype = ctypes.c_uint32
+            lib.oracle_order_key_batch.argtypes = [ctypes.c_void_p, ctypes.c_void_p,
+                                                   ctypes.c_int64]
+            lib.oracle_order_key_batch.restype = None
+            lib.oracle_topk_ragged.argtypes = [
+                ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                ctypes.c_int32, ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p,
+                ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int]
+            lib.oracle_topk_ragged.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def order_key(bits: np.ndarray) -> np.ndarray:
+    """Order keys of fp32 bit patterns (uint32 in, uint32 out)."""
+    bits = np.ascontiguousarray(bits, dtype=np.uint32)
+    out = np.empty_like(bits)
+    _load().oracle_order_key_batch(bits.ctypes.data, out.ctypes.data, bits.size)
+    return out
+
+
+def topk_ragged(scores: np.ndarray, row_starts: np.ndarray, lengths: np.ndarray,
+                k: int, offset_mode: int = 0, n_threads: int = 1,
+                with_values: bool = True):
+    """Oracle top-k over a flat ragged fp32 buffer.
+
+    Returns ``(out_idx int32[B, k], out_val float32[B, k] or None,
+    row_flags uint32[B])``.  Bit patterns of ``out_val`` are the input's.
+    """
+    scores = np.ascontiguousarray(scores, dtype=np.float32).reshape(-1)
+    row_starts = np.ascontiguousarray(row_starts, dtype=np.int32).reshape(-1)
+    lengths = np.ascontiguousarray(lengths, dtype=np.int32).reshape(-1)
+    B = row_starts.size
+    if lengths.size != B:
+        raise ValueError("row_starts and lengths differ in size")
+    out_idx = np.empty((B, k), dtype=np.int32)
+    out_val = np.empty((B, k), dtype=np.float32) if with_values else None
+    flags = np.empty(B, dtype=np.uint32)
+    rc = _load().oracle_topk_ragged(
+        scores.ctypes.data if scores.size else None, scores.size,
+        row_starts.ctypes.data, lengths.ctypes.data, B, k, offset_mode,
+        out_idx.ctypes.data, out_val.ctypes.data if with_values else None,
+        flags.ctypes.data, int(n_threads))
+    if rc == -1:
+        raise ValueError(f"oracle: invalid argument (k={k}, offset_mode={offset_mode})")
+    if rc != 0:
+        raise MemoryError("oracle: worker allocation failed")
+    return out_idx, out_val, flags
