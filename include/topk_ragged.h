@@ -1,0 +1,141 @@
+/*
+ * topk_ragged.h -- C ABI of the deterministic exact ragged top-k library.
+ *
+ * The operation is the index-selection step of a DSA/QSA sparse-attention
+ * lightning indexer: for each query row pick the k (default 2048, at most
+ * 4096) highest-scoring key positions.  Its definition follows sglang PR
+ * #31115 "Add opt-in deterministic CuTe-DSL DSA top-k backend" (PR summary;
+ * Modifications; the hardening commit):
+ *
+ *   - canonical order: score descending, ascending index on bitwise-equal
+ *     scores, so at the k-th boundary the smallest-index subset of the tie set
+ *     is kept and no candidate is ever dropped;
+ *   - the order on scores is the bitwise total order of fp32 patterns: each
+ *     pattern u maps to the unsigned key (u & 0x80000000) ? ~u : u | 0x80000000
+ *     and a larger key ranks first, so -NaN < -inf < ... < -0.0 < +0.0 < ...
+ *     < +inf < +NaN, with NaN payloads ordered by their bits (not torch.topk's
+ *     NaN-maximal order);
+ *   - output rows are front-packed: the min(k, L_i) selected indices in
+ *     canonical order, then -1.
+ *
+ * Every call is stream-ordered and asynchronous, allocates nothing, and may be
+ * captured into a CUDA graph once topk_ragged_init() has run for the device.
+ * Results are bitwise identical from run to run and independent of which
+ * other rows share the batch.
+ */
+#ifndef TOPK_RAGGED_H
+#define TOPK_RAGGED_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define TOPK_RAGGED_ABI_VERSION 1
+#define TOPK_RAGGED_MAX_K 4096
+/* Row lengths must stay below 2^24 (the pages' envelope "L < 2**24"). */
+#define TOPK_RAGGED_MAX_LEN (1 << 24)
+
+/* Synchronous return codes. */
+typedef enum {
+    TOPK_OK = 0,
+    TOPK_ERR_INVALID_ARG = 1,        /* an argument outside the contract below  */
+    TOPK_ERR_NOT_INITIALIZED = 2,    /* called under stream capture before init */
+    TOPK_ERR_UNSUPPORTED_DEVICE = 3, /* not a compute-capability 10.3 device    */
+    TOPK_ERR_CUDA = 4                /* a CUDA runtime call or launch failed    */
+} topk_status;
+
+/* offset_mode values. */
+enum {
+    TOPK_OFFSET_ROW_LOCAL = 0, /* out_idx holds j, the index inside the row      */
+    TOPK_OFFSET_ROW_START = 1  /* out_idx holds row_starts[i] + j (buffer index) */
+};
+
+/* Bits of the device status word (data errors found by the kernel). */
+enum {
+    TOPK_DEV_LEN_ENVELOPE = 1u, /* a row had lengths[i] >= 2^24; it was written as all -1   */
+    TOPK_DEV_BAD_WINDOW = 2u,   /* a row window left [0, n_scores); it was written as all -1 */
+    TOPK_DEV_INTERNAL = 4u      /* an internal consistency check failed (a library bug)      */
+};
+
+/* Version of this ABI (TOPK_RAGGED_ABI_VERSION). */
+int topk_ragged_abi_version(void);
+
+/* Static description of a status code; never NULL. */
+const char *topk_ragged_strerror(int status);
+
+/*
+ * Prepares `device` (0-based CUDA ordinal): checks that it is a
+ * compute-capability 10.3 GPU, sets the kernels' shared-memory and cluster
+ * attributes, and records the SM count used to size launches.  Idempotent and
+ * thread-safe.  Must run outside stream capture; topk_ragged() calls it
+ * itself on first use when the stream is not capturing.  Changes the calling
+ * thread's current device to `device` and does not restore it.
+ * Returns TOPK_OK, TOPK_ERR_UNSUPPORTED_DEVICE or TOPK_ERR_CUDA.
+ */
+int topk_ragged_init(int device);
+
+/*
+ * Exact top-k of every row of a flat ragged fp32 buffer (the
+ * `topk_func(score, lengths, topk, row_starts)` contract of the page above,
+ * with the 2-D score tensor replaced by one flat buffer and per-row windows).
+ *
+ * scores       device, fp32, n_scores entries, 4-byte aligned, read-only.
+ * n_scores     number of entries in `scores`, 0 <= n_scores < 2^31.  Every
+ *              row window must lie inside [0, n_scores); a row whose window
+ *              does not is written as all -1 and TOPK_DEV_BAD_WINDOW is set.
+ * row_starts   device, int32[B]: row i's window starts at scores[row_starts[i]].
+ * lengths      device, int32[B]: L_i = lengths[i]; a negative length reads as 0;
+ *              L_i >= 2^24 writes the row as all -1 and sets TOPK_DEV_LEN_ENVELOPE.
+ *              Windows may overlap, be unaligned and come in any order.
+ * B            number of rows, B >= 0; B == 0 returns TOPK_OK with no launch.
+ * k            1 <= k <= 4096, and (int64)B * k < 2^31.
+ * offset_mode  TOPK_OFFSET_ROW_LOCAL or TOPK_OFFSET_ROW_START.
+ * out_idx      device, int32[B, k] row-major, written entirely: row i holds
+ *              the min(k, L_i) selected indices in canonical order, then -1.
+ * out_val      device, fp32[B, k] or NULL: the selected scores' original bit
+ *              patterns (NaN payloads and the sign of zero survive), and -inf
+ *              in the -1 slots.
+ * stream       cudaStream_t to run on (NULL = legacy default stream).
+ *
+ * All buffers are owned by the caller and must stay valid until the stream
+ * reaches the call.  Output buffers must not overlap the inputs.  The call
+ * allocates no memory.  Returns TOPK_OK, TOPK_ERR_INVALID_ARG (nothing is
+ * launched), TOPK_ERR_NOT_INITIALIZED, TOPK_ERR_UNSUPPORTED_DEVICE or
+ * TOPK_ERR_CUDA.  Data errors are reported through
+ * topk_ragged_device_status().
+ */
+int topk_ragged(const float *scores, int64_t n_scores, const int32_t *row_starts,
+                const int32_t *lengths, int32_t B, int32_t k, int32_t offset_mode,
+                int32_t *out_idx, float *out_val, void *stream);
+
+/*
+ * Reads the current device's status word (an OR of TOPK_DEV_* bits from all
+ * calls since the last read) into *host_out, then clears it.  Synchronizes
+ * `stream`; not for use under stream capture.  Returns TOPK_OK,
+ * TOPK_ERR_INVALID_ARG (host_out NULL) or TOPK_ERR_CUDA.
+ */
+int topk_ragged_device_status(uint32_t *host_out, void *stream);
+
+/* How a call with these host arguments is launched on the current device. */
+typedef struct {
+    int32_t threads;        /* threads per CTA                                */
+    int32_t cluster;        /* CTAs per row (a thread-block cluster)          */
+    int32_t stage_cap;      /* scores per CTA held in shared memory           */
+    int32_t smem_bytes;     /* dynamic shared memory per CTA                  */
+    int32_t grid;           /* CTAs launched                                  */
+    int32_t launches;       /* kernel launches per call (0 when B == 0)       */
+} topk_launch_info;
+
+/*
+ * Fills *info for a call with (B, k) on the current device without launching
+ * anything.  Returns TOPK_OK, TOPK_ERR_INVALID_ARG or the init error.
+ */
+int topk_ragged_launch_info(int32_t B, int32_t k, topk_launch_info *info);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TOPK_RAGGED_H */

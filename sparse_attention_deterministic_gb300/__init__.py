@@ -1,0 +1,20 @@
+"""Deterministic exact ragged top-k for GB300 (sm_103a).
+
+The selection step of a sparse-attention lightning indexer: per ragged row of
+fp32 scores, the k best positions in canonical order (score descending under
+the bitwise fp32 total order, index ascending on bitwise-equal scores),
+-1 padded.  The work runs in the CUDA library built from ``csrc/`` and exposed
+through the C ABI in ``include/topk_ragged.h``; this package only builds,
+loads and calls it.
+"""
+from ._native import EXPORTS, LIB_PATH, TopkError, build, lib, strerror
+from .binding import (MAX_K, MAX_LEN, PAD_VALUE_BITS, TOPK_DEV_BAD_WINDOW,
+                      TOPK_DEV_INTERNAL, TOPK_DEV_LEN_ENVELOPE, TOPK_OFFSET_ROW_LOCAL,
+                      TOPK_OFFSET_ROW_START, device_status, init, launch_info, topk_ragged)
+
+__all__ = [
+    "EXPORTS", "LIB_PATH", "TopkError", "build", "lib", "strerror", "MAX_K", "MAX_LEN",
+    "PAD_VALUE_BITS", "TOPK_DEV_BAD_WINDOW", "TOPK_DEV_INTERNAL", "TOPK_DEV_LEN_ENVELOPE",
+    "TOPK_OFFSET_ROW_LOCAL", "TOPK_OFFSET_ROW_START", "device_status", "init", "launch_info",
+    "topk_ragged",
+]

@@ -1,0 +1,118 @@
+"""Python binding of the C ABI in ``include/topk_ragged.h``.
+
+Argument marshalling only: tensors are checked (dtype, device, layout) and
+their device pointers, sizes and the current CUDA stream are passed to the
+library.  Every step of the selection runs in the library's kernels; output
+tensors are allocated here with torch only when the caller does not pass them
+(the library call itself allocates nothing).
+"""
+from __future__ import annotations
+
+import ctypes
+
+import torch
+
+from ._native import LaunchInfo, TopkError, lib
+
+TOPK_OFFSET_ROW_LOCAL = 0
+TOPK_OFFSET_ROW_START = 1
+TOPK_DEV_LEN_ENVELOPE = 1
+TOPK_DEV_BAD_WINDOW = 2
+TOPK_DEV_INTERNAL = 4
+MAX_K = 4096
+MAX_LEN = 1 << 24
+PAD_VALUE_BITS = 0xFF800000
+
+
+def _stream_handle(device: torch.device, stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _check(t: torch.Tensor, name: str, dtype, device=None):
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.device.type != "cuda":
+        raise ValueError(f"{name} must be a CUDA tensor, got {t.device}")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+
+
+def init(device=None) -> None:
+    """Prepare a device (outside stream capture); see topk_ragged_init."""
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else
+                       torch.device(device).index or 0)
+    with torch.cuda.device(dev):
+        rc = lib().topk_ragged_init(dev.index)
+    if rc != 0:
+        raise TopkError(rc, "topk_ragged_init")
+
+
+def topk_ragged(scores: torch.Tensor, row_starts: torch.Tensor, lengths: torch.Tensor,
+                k: int = 2048, offset_mode: int = TOPK_OFFSET_ROW_LOCAL,
+                out_idx: torch.Tensor | None = None, out_val: torch.Tensor | None = None,
+                with_values: bool = False, stream=None):
+    """Deterministic exact top-k of each ragged row of a flat fp32 buffer.
+
+    scores      float32 CUDA tensor (any shape, contiguous; used as flat).
+    row_starts  int32 CUDA tensor [B]; lengths int32 CUDA tensor [B].
+    Returns (out_idx int32 [B, k], out_val float32 [B, k] or None).
+    """
+    _check(scores, "scores", torch.float32)
+    dev = scores.device
+    _check(row_starts, "row_starts", torch.int32, dev)
+    _check(lengths, "lengths", torch.int32, dev)
+    B = row_starts.numel()
+    if lengths.numel() != B:
+        raise ValueError(f"row_starts has {B} entries, lengths has {lengths.numel()}")
+    if out_idx is None:
+        out_idx = torch.empty((B, k), dtype=torch.int32, device=dev)
+    else:
+        _check(out_idx, "out_idx", torch.int32, dev)
+        if out_idx.numel() != B * k:
+            raise ValueError("out_idx must hold B * k entries")
+    if out_val is None and with_values:
+        out_val = torch.empty((B, k), dtype=torch.float32, device=dev)
+    elif out_val is not None:
+        _check(out_val, "out_val", torch.float32, dev)
+        if out_val.numel() != B * k:
+            raise ValueError("out_val must hold B * k entries")
+    with torch.cuda.device(dev):
+        rc = lib().topk_ragged(
+            scores.data_ptr() if scores.numel() else None, scores.numel(),
+            row_starts.data_ptr() if B else None, lengths.data_ptr() if B else None,
+            B, int(k), int(offset_mode), out_idx.data_ptr() if B else None,
+            out_val.data_ptr() if (out_val is not None and B) else None,
+            _stream_handle(dev, stream))
+    if rc != 0:
+        raise TopkError(rc, "topk_ragged")
+    return out_idx, out_val
+
+
+def device_status(device=None, stream=None) -> int:
+    """Read and clear the device status word (synchronises the stream)."""
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else
+                       torch.device(device).index or 0)
+    v = ctypes.c_uint32(0)
+    with torch.cuda.device(dev):
+        rc = lib().topk_ragged_device_status(ctypes.byref(v), _stream_handle(dev, stream))
+    if rc != 0:
+        raise TopkError(rc, "topk_ragged_device_status")
+    return int(v.value)
+
+
+def launch_info(B: int, k: int, device=None) -> dict:
+    """How (B, k) is launched on the device: threads, cluster, grid, ..."""
+    dev = torch.device("cuda", torch.cuda.current_device() if device is None else
+                       torch.device(device).index or 0)
+    info = LaunchInfo()
+    with torch.cuda.device(dev):
+        rc = lib().topk_ragged_launch_info(int(B), int(k), ctypes.byref(info))
+    if rc != 0:
+        raise TopkError(rc, "topk_ragged_launch_info")
+    return {name: int(getattr(info, name)) for name, _ in LaunchInfo._fields_}

@@ -1,0 +1,87 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every symbol the header declares, and rejects out-of-contract arguments before
+touching the device."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import sparse_attention_deterministic_gb300 as pkg
+from sparse_attention_deterministic_gb300 import _native
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def so():
+    pkg.build()
+    return pkg.lib()
+
+
+def _declared_functions():
+    names = []
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if not fn.endswith(".h"):
+            continue
+        text = open(os.path.join(ROOT, "include", fn)).read()
+        text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+        names += re.findall(r"\b(topk_ragged\w*)\s*\(", text)
+    return sorted(set(names))
+
+
+def test_exports_every_declared_symbol(so):
+    declared = _declared_functions()
+    assert declared, "no declarations found"
+    assert set(declared) == set(_native.EXPORTS)
+    for name in declared:
+        assert hasattr(so, name), name
+
+
+def test_abi_version_and_strerror(so):
+    assert so.topk_ragged_abi_version() == 1
+    for st in range(5):
+        assert pkg.strerror(st)
+    assert pkg.strerror(99) == "unknown status"
+
+
+def _call(so, scores=0x1000, n=16, rs=0x2000, ln=0x3000, B=1, k=4, mode=0, oi=0x4000):
+    return so.topk_ragged(scores, n, rs, ln, B, k, mode, oi, None, None)
+
+
+@pytest.mark.parametrize("kw", [
+    dict(k=0), dict(k=4097), dict(k=-1), dict(B=-1), dict(mode=2), dict(mode=-1),
+    dict(rs=None), dict(ln=None), dict(oi=None), dict(scores=None),
+    dict(scores=0x1002), dict(n=-1), dict(n=1 << 31), dict(B=1 << 20, k=4096),
+])
+def test_invalid_arguments_rejected_on_host(so, kw):
+    # Pointers here are never dereferenced: validation fails first.
+    assert _call(so, **kw) == 1
+
+
+def test_empty_batch_is_ok_without_device(so):
+    assert _call(so, B=0, rs=None, ln=None, oi=None, scores=None, n=0) == 0
+
+
+def test_device_status_null(so):
+    assert so.topk_ragged_device_status(None, None) == 1
+
+
+def test_launch_info_null(so):
+    assert so.topk_ragged_launch_info(4, 2048, None) == 1
+
+
+def test_header_defines_match_binding():
+    text = open(os.path.join(ROOT, "include", "topk_ragged.h")).read()
+    assert "#define TOPK_RAGGED_MAX_K 4096" in text
+    assert pkg.MAX_K == 4096 and pkg.MAX_LEN == 1 << 24
+    assert re.search(r"TOPK_DEV_LEN_ENVELOPE = 1u", text)
+    assert re.search(r"TOPK_DEV_BAD_WINDOW = 2u", text)
+    assert re.search(r"TOPK_DEV_INTERNAL = 4u", text)
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(_native, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(_native, "_lib", None)
+    with pytest.raises(RuntimeError, match="not built"):
+        _native.lib()
