@@ -15,8 +15,8 @@
 //     row and keeps as much of it as fits in shared memory, so the row is
 //     read from HBM once; the rest of a very long slice is re-read from L2;
 //   * an MSB-first radix select on the monotone uint32 order key with digits
-//     of 11, 11 and 10 bits; per-CTA histograms use warp-aggregated shared
-//     memory atomics (__match_any_sync) and are merged into the cluster
+//     of 11, 11 and 10 bits; per-CTA histograms use shared-memory atomics
+//     (colliding lanes are merged by the hardware) and are merged into the cluster
 //     leader through distributed shared memory (red.shared::cluster), so the
 //     k-th key T, the count above it and the count needed from its tie set
 //     are exact integers, independent of scheduling;
@@ -66,9 +66,14 @@ struct __align__(16) Ctrl {
     uint32_t sel_digit;  // result of the last threshold search
     uint32_t sel_gt;     //   entries above the chosen bin (within the prefix)
     uint32_t sel_cnt;    //   entries in the chosen bin
+    uint32_t sel_done;   //   1: the k-th key is +0.0 (plateau shortcut)
+    uint32_t zeros;      // this CTA's count of exact +0.0 scores
+    uint32_t zeros_tot;  // leader: the cluster's count of exact +0.0 scores
     uint32_t win_count;  // leader: winner slots handed out
+    uint32_t pad;
     uint32_t warp_ties[32];
-    uint32_t scan[32];
+    uint32_t scan[36];
+    uint32_t red[64];
 };
 
 // ------------------------------------------------------------------------- //
@@ -139,6 +144,11 @@ __device__ __forceinline__ uint32_t dsmem_atom_add(uint32_t addr, uint32_t v)
     return old;
 }
 
+__device__ __forceinline__ void dsmem_st64(uint32_t addr, uint64_t v)
+{
+    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+
 __device__ __forceinline__ uint32_t dsmem_ld(uint32_t addr)
 {
     uint32_t v;
@@ -149,11 +159,6 @@ __device__ __forceinline__ uint32_t dsmem_ld(uint32_t addr)
 __device__ __forceinline__ void dsmem_st(uint32_t addr, uint32_t v)
 {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ void dsmem_st64(uint32_t addr, uint64_t v)
-{
-    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
 }
 
 // ------------------------------------------------------------------------- //
@@ -190,15 +195,13 @@ __device__ __forceinline__ uint32_t block_incl_scan(uint32_t x, uint32_t *sm)
     return x;
 }
 
-// Warp-aggregated histogram increment: lanes holding the same digit are
-// merged with one match and the group leader adds the group size.  Every
-// lane of the warp must call this together.
+// Histogram increment.  On this GPU a shared-memory atomic add whose lanes
+// collide on one address is merged by the hardware at full rate, while
+// __match_any_sync is serialised per distinct value, so the plain per-lane
+// atomic is the cheapest form on every digit distribution, plateau included.
 __device__ __forceinline__ void hist_add(uint32_t *hist, uint32_t digit, bool valid)
 {
-    const uint32_t d = valid ? digit : kFull;
-    const uint32_t peers = __match_any_sync(kFull, d);
-    const int lane = threadIdx.x & 31;
-    if (valid && lane == __ffs(peers) - 1) atomicAdd(&hist[digit], (uint32_t)__popc(peers));
+    if (valid) atomicAdd(&hist[digit], 1u);
 }
 
 // ------------------------------------------------------------------------- //
@@ -252,32 +255,50 @@ __device__ __forceinline__ uint4 load_quad(const Slice &s, const uint32_t *keys,
 // ------------------------------------------------------------------------- //
 // Threshold search: given a histogram h over kBins digits (larger digit =
 // larger key) and r >= 1 entries still to take, find the bin b with
-// sum(h[> b]) < r <= sum(h[>= b]).  The single owning thread stores
-// (b, sum(h[> b]), h[b]) into out; the caller synchronises.
+// sum(h[> b]) < r <= sum(h[>= b]).  The single owning thread returns true
+// with (b, sum(h[> b]), h[b]); the caller publishes and synchronises.
+// Each thread owns BPT consecutive bins, read as 16-byte vectors.
 // ------------------------------------------------------------------------- //
+template <int THREADS>
+__device__ __forceinline__ void load_bins(const uint32_t *h, int lo, uint32_t (&v)[kBins / THREADS])
+{
+    constexpr int BPT = kBins / THREADS;
+    if constexpr (BPT % 4 == 0) {
+#pragma unroll
+        for (int i = 0; i < BPT; i += 4) {
+            const uint4 x = *reinterpret_cast<const uint4 *>(h + lo + i);
+            v[i] = x.x; v[i + 1] = x.y; v[i + 2] = x.z; v[i + 3] = x.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < BPT; i += 2) {
+            const uint2 x = *reinterpret_cast<const uint2 *>(h + lo + i);
+            v[i] = x.x; v[i + 1] = x.y;
+        }
+    }
+}
+
 template <int THREADS>
 __device__ __forceinline__ bool find_bin(const uint32_t *h, uint32_t r, uint32_t *sm,
                                          uint32_t &digit, uint32_t &gt, uint32_t &cnt)
 {
     constexpr int BPT = kBins / THREADS;
-    const int top = kBins - 1 - (int)threadIdx.x * BPT;
+    const int lo = kBins - ((int)threadIdx.x + 1) * BPT;   // thread 0 owns the top bins
     uint32_t v[BPT];
+    load_bins<THREADS>(h, lo, v);
     uint32_t sum = 0;
 #pragma unroll
-    for (int i = 0; i < BPT; ++i) {
-        v[i] = h[top - i];
-        sum += v[i];
-    }
+    for (int i = 0; i < BPT; ++i) sum += v[i];
     const uint32_t incl = block_incl_scan<THREADS>(sum, sm);
     const uint32_t excl = incl - sum;
     bool mine = false;
     if (excl < r && r <= incl) {
         uint32_t acc = excl;
 #pragma unroll
-        for (int i = 0; i < BPT; ++i) {
+        for (int i = BPT - 1; i >= 0; --i) {   // descending bins
             if (!mine && acc + v[i] >= r) {
                 mine = true;
-                digit = (uint32_t)(top - i);
+                digit = (uint32_t)(lo + i);
                 gt = acc;
                 cnt = v[i];
             }
@@ -288,7 +309,43 @@ __device__ __forceinline__ bool find_bin(const uint32_t *h, uint32_t r, uint32_t
 }
 
 // ------------------------------------------------------------------------- //
-// Descending bitonic sort of n = power of two composites in shared memory.
+// Block reductions (result valid in every thread; `sm` needs 32 words and
+// must not be reused before the next __syncthreads).
+// ------------------------------------------------------------------------- //
+template <int THREADS>
+__device__ __forceinline__ void block_minmax(uint32_t &mn, uint32_t &mx, uint32_t *sm)
+{
+    constexpr int NW = THREADS / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    mn = __reduce_min_sync(kFull, mn);
+    mx = __reduce_max_sync(kFull, mx);
+    if (lane == 0) {
+        sm[warp] = mn;
+        sm[32 + warp] = mx;
+    }
+    __syncthreads();
+    mn = __reduce_min_sync(kFull, lane < NW ? sm[lane] : kFull);
+    mx = __reduce_max_sync(kFull, lane < NW ? sm[32 + lane] : 0u);
+    __syncthreads();
+}
+
+template <int THREADS>
+__device__ __forceinline__ uint32_t block_sum(uint32_t x, uint32_t *sm)
+{
+    constexpr int NW = THREADS / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    x = __reduce_add_sync(kFull, x);
+    if (lane == 0) sm[warp] = x;
+    __syncthreads();
+    uint32_t a = lane < NW ? sm[lane] : 0u;
+    a = __reduce_add_sync(kFull, a);
+    __syncthreads();
+    return a;
+}
+
+// ------------------------------------------------------------------------- //
+// Descending bitonic sort of n = power of two composites (the fallback of
+// bucket_sort_desc for pathologically skewed key distributions).
 // ------------------------------------------------------------------------- //
 template <int THREADS>
 __device__ void bitonic_desc(uint64_t *a, uint32_t n)
@@ -310,6 +367,88 @@ __device__ void bitonic_desc(uint64_t *a, uint32_t n)
     }
 }
 
+// ------------------------------------------------------------------------- //
+// Sort n unique composites (key << 32 | ~index) in a[0..n) descending, i.e.
+// into canonical order.  The key range [kmin, kmax] of the winners is cut
+// into kBins buckets of 2^s keys (s chosen so the range spans at most kBins
+// buckets); bucket sizes come from a shared-memory histogram, buckets are
+// laid out in descending order by a scan, every composite is dropped into
+// its bucket (order inside a bucket is arbitrary), and its final position is
+// the bucket start plus the number of bucket members above it.  The result
+// depends only on the composites, never on the scatter order.  Work is
+// n + sum(m_b^2); when the buckets are too skewed for that to be small, the
+// function sorts with a bitonic network instead.  b[] is scratch of n
+// composites, cur[] kBins words, sm 32 and red 64 words.  The result is in a[].
+// ------------------------------------------------------------------------- //
+template <int THREADS>
+__device__ void bucket_sort_desc(uint64_t *a, uint64_t *b, int n, int cap_pow2, uint32_t *cur,
+                                 uint32_t *sm, uint32_t *red)
+{
+    constexpr int BPT = kBins / THREADS;
+    const int tid = threadIdx.x;
+    uint32_t mn = kFull, mx = 0;
+    for (int i = tid; i < n; i += THREADS) {
+        const uint32_t k = (uint32_t)(a[i] >> 32);
+        mn = min(mn, k);
+        mx = max(mx, k);
+    }
+    block_minmax<THREADS>(mn, mx, red);
+    const uint32_t range = mx - mn;
+    const int s = max(0, (32 - __clz(range)) - 11);
+    for (int i = tid; i < kBins; i += THREADS) cur[i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < n; i += THREADS) atomicAdd(&cur[((uint32_t)(a[i] >> 32) - mn) >> s], 1u);
+    __syncthreads();
+    const int lo = kBins - (tid + 1) * BPT;
+    uint32_t v[BPT];
+    load_bins<THREADS>(cur, lo, v);
+    uint32_t sum = 0, sq = 0;
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) {
+        sum += v[i];
+        sq += v[i] * v[i];
+    }
+    uint32_t run = block_incl_scan<THREADS>(sum, sm) - sum;
+#pragma unroll
+    for (int i = BPT - 1; i >= 0; --i) {
+        const uint32_t x = v[i];
+        v[i] = run;
+        run += x;
+    }
+    __syncthreads();
+    const uint32_t total_sq = block_sum<THREADS>(sq, sm);
+    if (total_sq > 32u * (uint32_t)n + 1024u) {
+        int n2 = 1;
+        while (n2 < n) n2 <<= 1;
+        if (n2 > cap_pow2) n2 = cap_pow2;   // n <= cap_pow2 always
+        for (int i = n + tid; i < n2; i += THREADS) a[i] = 0ull;
+        __syncthreads();
+        bitonic_desc<THREADS>(a, (uint32_t)n2);
+        return;
+    }
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) cur[lo + i] = v[i];   // bucket starts
+    __syncthreads();
+    for (int i = tid; i < n; i += THREADS) {
+        const uint64_t x = a[i];
+        const uint32_t pos = atomicAdd(&cur[((uint32_t)(x >> 32) - mn) >> s], 1u);
+        b[pos] = x;
+    }
+    __syncthreads();
+    // cur[d] is now the end of bucket d, and the start of bucket d is the
+    // end of bucket d + 1 (buckets are laid out from the top digit down).
+    for (int p = tid; p < n; p += THREADS) {
+        const uint64_t x = b[p];
+        const uint32_t d = ((uint32_t)(x >> 32) - mn) >> s;
+        const uint32_t st = d + 1 < (uint32_t)kBins ? cur[d + 1] : 0u;
+        const uint32_t en = cur[d];
+        uint32_t rank = 0;
+        for (uint32_t q = st; q < en; ++q) rank += b[q] > x;
+        a[st + rank] = x;
+    }
+    __syncthreads();
+}
+
 __device__ __forceinline__ void pad_out(int32_t *oi, float *ov, int from, int to)
 {
     for (int p = from + (int)threadIdx.x; p < to; p += (int)blockDim.x) {
@@ -322,10 +461,13 @@ __device__ __forceinline__ void pad_out(int32_t *oi, float *ov, int from, int to
 // The kernel: one row per cluster (CLUSTER) or per CTA.
 // ------------------------------------------------------------------------- //
 template <int THREADS, bool CLUSTER>
-__global__ void __launch_bounds__(THREADS, CLUSTER ? 1 : 4) topk_ragged_kernel(const Params p)
+__global__ void __launch_bounds__(THREADS, CLUSTER ? 2048 / THREADS / 2 : 2048 / THREADS / 2)
+topk_ragged_kernel(const Params p)
 {
     constexpr int NW = THREADS / 32;
-    constexpr int U = 4;   // quads in flight per lane in the streaming pass
+    constexpr int U = 4;                       // quads in flight per lane in the streaming pass
+    constexpr uint32_t kZeroKey = 0x80000000u; // order key of +0.0
+    constexpr uint32_t kZeroDigit = kZeroKey >> 21;
     extern __shared__ __align__(16) unsigned char smem[];
     Ctrl &ctrl = *reinterpret_cast<Ctrl *>(smem);
     uint32_t *hist = reinterpret_cast<uint32_t *>(smem + sizeof(Ctrl));
@@ -389,20 +531,20 @@ __global__ void __launch_bounds__(THREADS, CLUSTER ? 1 : 4) topk_ragged_kernel(c
         if (CLUSTER && leader) hist_tot[b] = 0u;
     }
     if (tid == 0) {
-        ctrl.win_count = 0u;
         ctrl.sel_digit = 0u;
         ctrl.sel_gt = 0u;
         ctrl.sel_cnt = 0u;
+        ctrl.sel_done = 0u;
+        ctrl.zeros = 0u;
+        ctrl.zeros_tot = 0u;
+        ctrl.win_count = 0u;
     }
     __syncthreads();
     if (CLUSTER) cluster_arrive();   // B0: every CTA started and zeroed (waited before the flush)
 
-    const uint32_t lead_hist_tot = CLUSTER ? dsmem_addr(hist_tot, 0) : 0u;
-
-    // Running selection state (identical in every thread of the cluster).
-    uint32_t prefix = 0, n_gt = 0, r = k_eff, cnt = 0;
-
-    // ---- a2+a3: stream the slice once: key transform, stage, top-digit hist //
+    // ---- a2+a3: stream the slice once: key transform, stage, top-digit
+    //      histogram, and a count of exact +0.0 (the ReLU plateau) --------- //
+    uint32_t zeros = 0;
     for (int qb = warp * 32 * U; qb < s.nq; qb += THREADS * U) {
         uint4 kk[U];
         uint32_t m[U];
@@ -412,15 +554,25 @@ __global__ void __launch_bounds__(THREADS, CLUSTER ? 1 : 4) topk_ragged_kernel(c
         for (int u = 0; u < U; ++u) {
             const int q = qb + u * 32 + lane;
             if (q < s.sq) reinterpret_cast<uint4 *>(keys)[q] = kk[u];
+            zeros += ((m[u] & 1u) && kk[u].x == kZeroKey) + ((m[u] & 2u) && kk[u].y == kZeroKey) +
+                     ((m[u] & 4u) && kk[u].z == kZeroKey) + ((m[u] & 8u) && kk[u].w == kZeroKey);
             hist_add(hist, kk[u].x >> 21, m[u] & 1u);
             hist_add(hist, kk[u].y >> 21, m[u] & 2u);
             hist_add(hist, kk[u].z >> 21, m[u] & 4u);
             hist_add(hist, kk[u].w >> 21, m[u] & 8u);
         }
     }
+    zeros = __reduce_add_sync(kFull, zeros);
+    if (lane == 0 && zeros) atomicAdd(&ctrl.zeros, zeros);
     __syncthreads();
 
-    // ---- a4+a5: three radix levels (11, 11, 10 bits) ---------------------- //
+    const uint32_t lead_hist_tot = CLUSTER ? dsmem_addr(hist_tot, 0) : 0u;
+
+    // Running selection state (identical in every thread of the cluster).
+    uint32_t prefix = 0, n_gt = 0, r = k_eff, cnt = 0;
+    bool plateau = false;   // T is +0.0, found from the zero count
+
+    // ---- a4+a5: radix levels of 11, 11 and 10 bits ------------------------ //
 #pragma unroll 1
     for (int level = 0; level < 3; ++level) {
         const int dbits = level == 2 ? 10 : 11;
@@ -435,48 +587,58 @@ __global__ void __launch_bounds__(THREADS, CLUSTER ? 1 : 4) topk_ragged_kernel(c
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const bool v = ((m >> i) & 1u) && (e[i] >> pshift) == prefix;
-                    if (__any_sync(kFull, v)) hist_add(hist, (e[i] >> dshift) & dmask, v);
+                    hist_add(hist, (e[i] >> dshift) & dmask, v);
                 }
             }
             __syncthreads();
         }
         uint32_t d = 0, gt = 0, c = 0;
+        const uint32_t *htot = hist;
         if (CLUSTER) {
             if (level == 0) cluster_wait();   // B0 complete: the leader's totals are zeroed
             for (int b = tid; b < kBins; b += THREADS) {
                 const uint32_t v = hist[b];
                 if (v) dsmem_red_add(lead_hist_tot + 4u * (uint32_t)b, v);
             }
+            if (level == 0 && tid == 0 && ctrl.zeros)
+                dsmem_red_add(dsmem_addr(&ctrl.zeros_tot, 0), ctrl.zeros);
             cluster_sync();   // B1: the leader holds the cluster-wide histogram
-            if (leader) {
-                if (find_bin<THREADS>(hist_tot, r, ctrl.scan, d, gt, c)) {
+            htot = hist_tot;
+        }
+        if (!CLUSTER || leader) {
+            if (find_bin<THREADS>(htot, r, ctrl.scan, d, gt, c)) {
+                // Plateau shortcut: the boundary bin holds only exact +0.0, so
+                // the k-th key is +0.0 and the finer levels are not needed.
+                const uint32_t ztot = CLUSTER ? ctrl.zeros_tot : ctrl.zeros;
+                const uint32_t done = (level == 0 && d == kZeroDigit && c == ztot) ? 1u : 0u;
+                if (CLUSTER) {
                     for (uint32_t rk = 0; rk < csize; ++rk) {
                         dsmem_st(dsmem_addr(&ctrl.sel_digit, rk), d);
                         dsmem_st(dsmem_addr(&ctrl.sel_gt, rk), gt);
                         dsmem_st(dsmem_addr(&ctrl.sel_cnt, rk), c);
+                        dsmem_st(dsmem_addr(&ctrl.sel_done, rk), done);
                     }
+                } else {
+                    ctrl.sel_digit = d;
+                    ctrl.sel_gt = gt;
+                    ctrl.sel_cnt = c;
+                    ctrl.sel_done = done;
                 }
+            }
+        }
+        if (CLUSTER) {
+            if (leader) {
                 __syncthreads();
                 for (int b = tid; b < kBins; b += THREADS) hist_tot[b] = 0u;
-            } else if (level < 2) {
-                for (int b = tid; b < kBins; b += THREADS) hist[b] = 0u;
             }
             cluster_sync();   // B2: selection visible everywhere
-            if (leader && level < 2)
-                for (int b = tid; b < kBins; b += THREADS) hist[b] = 0u;
         } else {
-            if (find_bin<THREADS>(hist, r, ctrl.scan, d, gt, c)) {
-                ctrl.sel_digit = d;
-                ctrl.sel_gt = gt;
-                ctrl.sel_cnt = c;
-            }
             __syncthreads();
-            if (level < 2)
-                for (int b = tid; b < kBins; b += THREADS) hist[b] = 0u;
         }
         d = ctrl.sel_digit;
         gt = ctrl.sel_gt;
         c = ctrl.sel_cnt;
+        const bool done = ctrl.sel_done != 0u;
         // Exact integer counts guarantee gt < r <= gt + c; anything else is a
         // library bug: flag it and keep every later write inside the row.
         if (gt >= r || r - gt > c) {
@@ -484,26 +646,40 @@ __global__ void __launch_bounds__(THREADS, CLUSTER ? 1 : 4) topk_ragged_kernel(c
             gt = r - 1u;
             c = 1u;
         }
-        prefix = (prefix << dbits) | d;
         n_gt += gt;
         r -= gt;
         cnt = c;
+        if (done) {
+            prefix = kZeroKey;
+            plateau = true;
+            __syncthreads();
+            break;
+        }
+        prefix = (prefix << dbits) | d;
+        if (level < 2)
+            for (int b = tid; b < kBins; b += THREADS) hist[b] = 0u;
         __syncthreads();
     }
     const uint32_t T = prefix;   // exact k-th key; n_gt above it, take r of its cnt ties
 
-    // ---- a6: winners (key > T) to the leader, tie counts per warp ---------- //
+    // ---- a6: winners (key > T) go to the leader's list in any order (their
+    //      composites are unique, the sort makes the order canonical); ties
+    //      (key == T) are counted per warp over contiguous warp segments. --- //
     uint32_t tie_base = 0, local_eq = cnt;
     if (CLUSTER) {
-        local_eq = hist[T & 0x3FFu];   // this CTA's level-3 histogram is intact
+        local_eq = plateau ? ctrl.zeros : hist[T & 0x3FFu];
         uint32_t part = 0;
-        if (warp == 0 && lane < (int)crank) part = dsmem_ld(dsmem_addr(&hist[T & 0x3FFu], (uint32_t)lane));
+        if (warp == 0 && lane < (int)crank) {
+            const void *src = plateau ? (const void *)&ctrl.zeros : (const void *)&hist[T & 0x3FFu];
+            part = dsmem_ld(dsmem_addr(src, (uint32_t)lane));
+        }
         if (warp == 0) part = __reduce_add_sync(kFull, part);
         if (tid == 0) ctrl.scan[0] = part;
         __syncthreads();
         tie_base = ctrl.scan[0];
         __syncthreads();
     }
+    const bool want_ties = local_eq > 0 && tie_base < r;   // CTA-uniform
     const uint32_t win_count_addr = CLUSTER ? dsmem_addr(&ctrl.win_count, 0) : 0u;
     const uint32_t win_addr = CLUSTER ? dsmem_addr(win, 0) : 0u;
     const int per_warp = (s.nq + NW - 1) / NW;
@@ -516,22 +692,23 @@ __global__ void __launch_bounds__(THREADS, CLUSTER ? 1 : 4) topk_ragged_kernel(c
         uint4 kk = make_uint4(0, 0, 0, 0);
         if (q < wq1) kk = load_quad(s, keys, q, m);
         const uint32_t e[4] = {kk.x, kk.y, kk.z, kk.w};
-        uint32_t wm = 0, tm = 0;
+        uint32_t wm = 0, tc = 0;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            if ((m >> i) & 1u) {
-                if (e[i] > T) wm |= 1u << i;
-                else if (e[i] == T) tm |= 1u << i;
-            }
+            const bool v = (m >> i) & 1u;
+            if (v && e[i] > T) wm |= 1u << i;
+            tc += v && e[i] == T;
         }
+        if (want_ties) ties_w += __reduce_add_sync(kFull, tc);
         const uint32_t wc = (uint32_t)__popc(wm);
-        const uint32_t wincl = warp_incl_scan(wc);
-        const uint32_t wtot = __shfl_sync(kFull, wincl, 31);
-        if (wtot) {
+        const uint32_t any = __ballot_sync(kFull, wc != 0);
+        if (any) {
+            const uint32_t wincl = warp_incl_scan(wc);
+            const uint32_t wtot = __shfl_sync(kFull, wincl, 31);
             uint32_t base = 0;
-            if (lane == 0)
+            if (lane == 31)
                 base = CLUSTER ? dsmem_atom_add(win_count_addr, wtot) : atomicAdd(&ctrl.win_count, wtot);
-            base = __shfl_sync(kFull, base, 0);
+            base = __shfl_sync(kFull, base, 31);
             uint32_t slot = base + wincl - wc;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
@@ -546,66 +723,70 @@ __global__ void __launch_bounds__(THREADS, CLUSTER ? 1 : 4) topk_ragged_kernel(c
                 }
             }
         }
-        ties_w += __reduce_add_sync(kFull, (uint32_t)__popc(tm));
     }
-    if (lane == 0) ctrl.warp_ties[warp] = ties_w;
-    __syncthreads();
 
-    // ---- a7: boundary ties in index order: ordinal o < r goes to n_gt + o -- //
-    if (local_eq > 0 && tie_base < r) {
+    // ---- a7: the first r ties in cluster-wide index order go to positions
+    //      n_gt + ordinal (their canonical place, right after the winners) -- //
+    if (want_ties) {
+        if (lane == 0) ctrl.warp_ties[warp] = ties_w;
+        __syncthreads();
         if (warp == 0) {
-            const uint32_t v = lane < NW ? ctrl.warp_ties[lane] : 0u;
-            const uint32_t incl = warp_incl_scan(v);
-            if (lane < NW) ctrl.warp_ties[lane] = incl - v;
+            const uint32_t b = lane < NW ? ctrl.warp_ties[lane] : 0u;
+            const uint32_t bi = warp_incl_scan(b);
+            if (lane < NW) ctrl.warp_ties[lane] = bi - b;
         }
         __syncthreads();
-        uint32_t run = tie_base + ctrl.warp_ties[warp];
+        uint32_t trun = tie_base + ctrl.warp_ties[warp];
         const uint32_t tval = key_bits(T);
-        for (int qb = wq0; qb < wq1 && run < r; qb += 32) {
-            const int q = qb + lane;
-            uint32_t m = 0;
-            uint4 kk = make_uint4(0, 0, 0, 0);
-            if (q < wq1) kk = load_quad(s, keys, q, m);
-            const uint32_t e[4] = {kk.x, kk.y, kk.z, kk.w};
-            uint32_t tm = 0;
+        if (ties_w > 0 && trun < r) {   // warp-uniform
+            for (int qb = wq0; qb < wq1 && trun < r; qb += 32) {
+                const int q = qb + lane;
+                uint32_t m = 0;
+                uint4 kk = make_uint4(0, 0, 0, 0);
+                if (q < wq1) kk = load_quad(s, keys, q, m);
+                const uint32_t e[4] = {kk.x, kk.y, kk.z, kk.w};
+                uint32_t tm = 0;
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                if (((m >> i) & 1u) && e[i] == T) tm |= 1u << i;
-            const uint32_t tc = (uint32_t)__popc(tm);
-            const uint32_t incl = warp_incl_scan(tc);
-            uint32_t ord = run + incl - tc;
+                for (int i = 0; i < 4; ++i)
+                    if (((m >> i) & 1u) && e[i] == T) tm |= 1u << i;
+                const uint32_t tc = (uint32_t)__popc(tm);
+                const uint32_t tb = __ballot_sync(kFull, tc != 0);
+                if (tb) {
+                    const uint32_t tincl = warp_incl_scan(tc);
+                    uint32_t tord = trun + tincl - tc;
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                if ((tm >> i) & 1u) {
-                    if (ord < r && n_gt + ord < k_eff) {
-                        const int32_t j = s.jbase + 4 * q + i;
-                        const uint32_t pos = n_gt + ord;
-                        oi[pos] = p.offset_mode == TOPK_OFFSET_ROW_START ? (int32_t)(rs + j) : j;
-                        if (ov) ov[pos] = __uint_as_float(tval);
+                    for (int i = 0; i < 4; ++i) {
+                        if ((tm >> i) & 1u) {
+                            if (tord < r && n_gt + tord < k_eff) {
+                                const int32_t j = s.jbase + 4 * q + i;
+                                const uint32_t pos = n_gt + tord;
+                                oi[pos] = p.offset_mode == TOPK_OFFSET_ROW_START ? (int32_t)(rs + j) : j;
+                                if (ov) ov[pos] = __uint_as_float(tval);
+                            }
+                            ++tord;
+                        }
                     }
-                    ++ord;
+                    trun += __shfl_sync(kFull, tincl, 31);
                 }
             }
-            run += __shfl_sync(kFull, incl, 31);
         }
     }
 
-    // ---- a8+a9: leader sorts the winners and writes the row --------------- //
-    if (CLUSTER) cluster_sync();   // B3: all winners delivered
-    else __syncthreads();
-    if (!leader) return;
-
+    // ---- a8+a9: the leader sorts the winners and writes the row ----------- //
+    if (CLUSTER) {
+        cluster_sync();   // B3: every winner is in the leader's list
+        if (!leader) return;
+    } else {
+        __syncthreads();
+    }
     const uint32_t n_win = ctrl.win_count;
     if (n_win != n_gt || n_gt > (uint32_t)p.win_cap) {
         if (tid == 0) atomicOr(&g_status, TOPK_DEV_INTERNAL);
     }
     const uint32_t n_sort = n_gt < (uint32_t)p.win_cap ? n_gt : (uint32_t)p.win_cap;
     if (n_sort > 0) {
-        uint32_t n2 = 1;
-        while (n2 < n_sort) n2 <<= 1;
-        for (uint32_t i = n_sort + tid; i < n2; i += THREADS) win[i] = 0ull;
-        __syncthreads();
-        bitonic_desc<THREADS>(win, n2);
+        bucket_sort_desc<THREADS>(win, reinterpret_cast<uint64_t *>(keys), (int)n_sort, p.win_cap,
+                                  hist, ctrl.scan, ctrl.red);
         for (uint32_t pidx = tid; pidx < n_sort; pidx += THREADS) {
             const uint64_t c = win[pidx];
             const int32_t j = (int32_t)(~(uint32_t)c);
@@ -637,7 +818,10 @@ struct DeviceInfo {
     bool ready = false;
     int status = TOPK_OK;
     int sm_count = 0;
-    int max_smem = 0;   // opt-in dynamic shared memory per block
+    int max_smem = 0;      // opt-in dynamic shared memory per block
+    int smem_per_sm = 0;   // shared memory per multiprocessor
+    // max_clusters[variant][C]: co-resident clusters of C CTAs (0 = not launchable)
+    int max_clusters[3][17] = {};
 };
 
 std::mutex g_mutex;
@@ -664,20 +848,36 @@ int header_bytes(bool cluster)
     return (int)sizeof(Ctrl) + kBins * 4 * (cluster ? 2 : 1);
 }
 
+// Launch shape from the host arguments alone (row lengths live on the
+// device and are never read here).  Large batches get one 256-thread CTA per
+// row, several CTAs per SM.  Smaller batches get a cluster of C CTAs per row,
+// C the largest power of two <= 16 that keeps the whole grid resident in one
+// wave at two 512-thread CTAs per SM; batches that fit 16-CTA clusters at one
+// CTA per SM use 1024-thread CTAs with all of an SM's shared memory, which
+// gives very long rows the most staging space.  Each CTA stages what shared
+// memory allows and re-reads the rest of its slice from L2.
 Plan make_plan(int32_t B, int32_t k, const DeviceInfo &dev)
 {
     Plan pl{};
     pl.win_cap = next_pow2(k - 1 > 1 ? k - 1 : 1);
     const int sms = dev.sm_count;
-    int vi, cluster, stage_cap;
+    int vi, cluster, smem_budget;
     if (B >= 4 * sms) {
-        vi = 0; cluster = 1; stage_cap = 4096 + 256;
-    } else if (B >= sms) {
-        vi = 1; cluster = 2; stage_cap = 16384;
-    } else if (4 * B >= sms) {
-        vi = 1; cluster = 8; stage_cap = 8192;
+        vi = 0;
+        cluster = 1;
+        smem_budget = 0;
     } else {
-        vi = 2; cluster = 16; stage_cap = 0;   // filled from the remaining smem
+        cluster = 1;
+        while (cluster < 16 && (int64_t)B * cluster * 2 <= 2 * (int64_t)sms &&
+               dev.max_clusters[1][cluster * 2] > 0)
+            cluster *= 2;
+        if (cluster == 16 && B * 16 <= sms && dev.max_clusters[2][16] > 0) {
+            vi = 2;
+            smem_budget = dev.max_smem;
+        } else {
+            vi = 1;
+            smem_budget = dev.smem_per_sm / 2 - 1024;
+        }
     }
     pl.v = &kVariants[vi];
     pl.cluster = cluster;
@@ -685,7 +885,9 @@ Plan make_plan(int32_t B, int32_t k, const DeviceInfo &dev)
     // The staged keys are read as 16-byte vectors: keep them 128-byte aligned
     // whatever the winner array's size (k <= 2 gives a single 8-byte slot).
     pl.off_keys = (pl.off_win + pl.win_cap * 8 + 127) & ~127;
-    if (stage_cap == 0) stage_cap = ((dev.max_smem - pl.off_keys) / 4) & ~127;
+    int stage_cap = smem_budget > 0 ? ((smem_budget - pl.off_keys) / 4) & ~127 : 4096 + 256;
+    // The staging area doubles as the sort's second buffer after compaction.
+    if (stage_cap < 2 * pl.win_cap) stage_cap = 2 * pl.win_cap;
     pl.stage_cap = stage_cap;
     pl.smem = pl.off_keys + stage_cap * 4;
     pl.grid = B * cluster;
@@ -712,6 +914,9 @@ int init_locked(int device)
     if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
         cudaDeviceGetAttribute(&d.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess)
         rc = TOPK_ERR_CUDA;
+    if (rc == TOPK_OK &&
+        cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device) != cudaSuccess)
+        rc = TOPK_ERR_CUDA;
     for (const Variant &v : kVariants) {
         if (rc != TOPK_OK) break;
         if (cudaFuncSetAttribute((const void *)v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -720,6 +925,32 @@ int init_locked(int device)
         if (v.cluster && cudaFuncSetAttribute((const void *)v.fn,
                                               cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
             rc = TOPK_ERR_CUDA;
+    }
+    // Which cluster sizes each clustered variant can actually co-schedule
+    // with the shared memory the planner gives it.
+    for (int vi = 1; vi < 3 && rc == TOPK_OK; ++vi) {
+        const Variant &v = kVariants[vi];
+        const int smem = vi == 2 ? d.max_smem : d.smem_per_sm / 2 - 1024;
+        for (int c = 2; c <= 16; c *= 2) {
+            cudaLaunchConfig_t cfg = {};
+            cfg.gridDim = dim3((unsigned)(c * 8), 1, 1);
+            cfg.blockDim = dim3((unsigned)v.threads, 1, 1);
+            cfg.dynamicSmemBytes = (size_t)smem;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeClusterDimension;
+            attr[0].val.clusterDim.x = (unsigned)c;
+            attr[0].val.clusterDim.y = 1;
+            attr[0].val.clusterDim.z = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, (const void *)v.fn, &cfg) != cudaSuccess) {
+                cudaGetLastError();
+                n = 0;
+            }
+            d.max_clusters[vi][c] = n;
+        }
+        d.max_clusters[vi][1] = 1;
     }
     cudaSetDevice(prev);
     if (rc == TOPK_OK) {
