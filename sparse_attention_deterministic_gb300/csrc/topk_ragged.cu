@@ -71,9 +71,14 @@ struct __align__(16) Ctrl {
     uint32_t zeros_tot;  // leader: the cluster's count of exact +0.0 scores
     uint32_t win_count;  // leader: winner slots handed out
     uint32_t pad;
+    uint32_t kmax;       // this CTA's largest order key
+    uint32_t kmax_tot;   // leader: the cluster's largest order key
+    uint32_t wmin;       // leader: the smallest winner key
+    uint32_t pad2;
+    uint32_t warp_zeros[32];
     uint32_t warp_ties[32];
     uint32_t scan[36];
-    uint32_t red[64];
+    uint64_t scan64[32];
 };
 
 // ------------------------------------------------------------------------- //
@@ -147,6 +152,16 @@ __device__ __forceinline__ uint32_t dsmem_atom_add(uint32_t addr, uint32_t v)
 __device__ __forceinline__ void dsmem_st64(uint32_t addr, uint64_t v)
 {
     asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ void dsmem_red_max(uint32_t addr, uint32_t v)
+{
+    asm volatile("red.shared::cluster.max.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ void dsmem_red_min(uint32_t addr, uint32_t v)
+{
+    asm volatile("red.shared::cluster.min.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ uint32_t dsmem_ld(uint32_t addr)
@@ -309,41 +324,6 @@ __device__ __forceinline__ bool find_bin(const uint32_t *h, uint32_t r, uint32_t
 }
 
 // ------------------------------------------------------------------------- //
-// Block reductions (result valid in every thread; `sm` needs 32 words and
-// must not be reused before the next __syncthreads).
-// ------------------------------------------------------------------------- //
-template <int THREADS>
-__device__ __forceinline__ void block_minmax(uint32_t &mn, uint32_t &mx, uint32_t *sm)
-{
-    constexpr int NW = THREADS / 32;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    mn = __reduce_min_sync(kFull, mn);
-    mx = __reduce_max_sync(kFull, mx);
-    if (lane == 0) {
-        sm[warp] = mn;
-        sm[32 + warp] = mx;
-    }
-    __syncthreads();
-    mn = __reduce_min_sync(kFull, lane < NW ? sm[lane] : kFull);
-    mx = __reduce_max_sync(kFull, lane < NW ? sm[32 + lane] : 0u);
-    __syncthreads();
-}
-
-template <int THREADS>
-__device__ __forceinline__ uint32_t block_sum(uint32_t x, uint32_t *sm)
-{
-    constexpr int NW = THREADS / 32;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    x = __reduce_add_sync(kFull, x);
-    if (lane == 0) sm[warp] = x;
-    __syncthreads();
-    uint32_t a = lane < NW ? sm[lane] : 0u;
-    a = __reduce_add_sync(kFull, a);
-    __syncthreads();
-    return a;
-}
-
-// ------------------------------------------------------------------------- //
 // Descending bitonic sort of n = power of two composites (the fallback of
 // bucket_sort_desc for pathologically skewed key distributions).
 // ------------------------------------------------------------------------- //
@@ -368,70 +348,94 @@ __device__ void bitonic_desc(uint64_t *a, uint32_t n)
 }
 
 // ------------------------------------------------------------------------- //
-// Sort n unique composites (key << 32 | ~index) in a[0..n) descending, i.e.
-// into canonical order.  The key range [kmin, kmax] of the winners is cut
-// into kBins buckets of 2^s keys (s chosen so the range spans at most kBins
-// buckets); bucket sizes come from a shared-memory histogram, buckets are
-// laid out in descending order by a scan, every composite is dropped into
-// its bucket (order inside a bucket is arbitrary), and its final position is
-// the bucket start plus the number of bucket members above it.  The result
-// depends only on the composites, never on the scatter order.  Work is
-// n + sum(m_b^2); when the buckets are too skewed for that to be small, the
-// function sorts with a bitonic network instead.  b[] is scratch of n
-// composites, cur[] kBins words, sm 32 and red 64 words.  The result is in a[].
+// 64-bit inclusive block scan (two 32-bit counters packed in one word); the
+// CTA-wide total is returned in `total`.  `sm` holds 32 64-bit words.
 // ------------------------------------------------------------------------- //
 template <int THREADS>
-__device__ void bucket_sort_desc(uint64_t *a, uint64_t *b, int n, int cap_pow2, uint32_t *cur,
-                                 uint32_t *sm, uint32_t *red)
+__device__ __forceinline__ uint64_t block_incl_scan64(uint64_t x, uint64_t *sm, uint64_t &total)
+{
+    constexpr int NW = THREADS / 32;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint64_t y = __shfl_up_sync(kFull, x, o);
+        if (lane >= o) x += y;
+    }
+    if (lane == 31) sm[warp] = x;
+    __syncthreads();
+    if (warp == 0) {
+        uint64_t w = lane < NW ? sm[lane] : 0ull;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint64_t y = __shfl_up_sync(kFull, w, o);
+            if (lane >= o) w += y;
+        }
+        if (lane < NW) sm[lane] = w;
+    }
+    __syncthreads();
+    if (warp > 0) x += sm[warp - 1];
+    total = sm[NW - 1];
+    return x;
+}
+
+// ------------------------------------------------------------------------- //
+// Sort the n unique composites (key << 32 | ~index) of a[0..n), all with
+// keys in [kmin, kmax], into canonical order (composite descending) and
+// write them to the output row.  The key range is cut into kBins buckets of
+// 2^s keys; bucket sizes come from a shared-memory histogram and are laid
+// out from the top bucket down by a scan; every composite is dropped into its
+// bucket (order inside a bucket is arbitrary) and its final position is the
+// bucket start plus the number of bucket members above it, so the result
+// depends only on the composites.  Work is n + sum(m_b^2); when the buckets
+// are too skewed for that to stay small the function sorts with a bitonic
+// network instead.  b[] is scratch for n composites, cur[] kBins words.
+// ------------------------------------------------------------------------- //
+template <int THREADS>
+__device__ void sort_and_write(uint64_t *a, uint64_t *b, int n, int cap_pow2, uint32_t kmin,
+                               uint32_t kmax, uint32_t *cur, uint64_t *sm64, int32_t *oi, float *ov,
+                               int64_t idx_offset)
 {
     constexpr int BPT = kBins / THREADS;
     const int tid = threadIdx.x;
-    uint32_t mn = kFull, mx = 0;
-    for (int i = tid; i < n; i += THREADS) {
-        const uint32_t k = (uint32_t)(a[i] >> 32);
-        mn = min(mn, k);
-        mx = max(mx, k);
-    }
-    block_minmax<THREADS>(mn, mx, red);
-    const uint32_t range = mx - mn;
+    const uint32_t range = kmax - kmin;
     const int s = max(0, (32 - __clz(range)) - 11);
     for (int i = tid; i < kBins; i += THREADS) cur[i] = 0u;
     __syncthreads();
-    for (int i = tid; i < n; i += THREADS) atomicAdd(&cur[((uint32_t)(a[i] >> 32) - mn) >> s], 1u);
+    for (int i = tid; i < n; i += THREADS) atomicAdd(&cur[((uint32_t)(a[i] >> 32) - kmin) >> s], 1u);
     __syncthreads();
     const int lo = kBins - (tid + 1) * BPT;
     uint32_t v[BPT];
     load_bins<THREADS>(cur, lo, v);
-    uint32_t sum = 0, sq = 0;
+    uint64_t pair = 0;   // (sum of squares << 32) | count
 #pragma unroll
-    for (int i = 0; i < BPT; ++i) {
-        sum += v[i];
-        sq += v[i] * v[i];
-    }
-    uint32_t run = block_incl_scan<THREADS>(sum, sm) - sum;
-#pragma unroll
-    for (int i = BPT - 1; i >= 0; --i) {
-        const uint32_t x = v[i];
-        v[i] = run;
-        run += x;
-    }
-    __syncthreads();
-    const uint32_t total_sq = block_sum<THREADS>(sq, sm);
-    if (total_sq > 32u * (uint32_t)n + 1024u) {
+    for (int i = 0; i < BPT; ++i) pair += ((uint64_t)(v[i] * v[i]) << 32) | v[i];
+    uint64_t total;
+    const uint64_t incl = block_incl_scan64<THREADS>(pair, sm64, total);
+    uint32_t run = (uint32_t)(incl - pair);
+    const uint32_t total_sq = (uint32_t)(total >> 32);
+    if (total_sq > 256u * (uint32_t)n + 4096u) {
         int n2 = 1;
         while (n2 < n) n2 <<= 1;
         if (n2 > cap_pow2) n2 = cap_pow2;   // n <= cap_pow2 always
         for (int i = n + tid; i < n2; i += THREADS) a[i] = 0ull;
         __syncthreads();
         bitonic_desc<THREADS>(a, (uint32_t)n2);
+        for (int p = tid; p < n; p += THREADS) {
+            const uint64_t c = a[p];
+            oi[p] = (int32_t)(idx_offset + (int32_t)(~(uint32_t)c));
+            if (ov) ov[p] = __uint_as_float(key_bits((uint32_t)(c >> 32)));
+        }
         return;
     }
 #pragma unroll
-    for (int i = 0; i < BPT; ++i) cur[lo + i] = v[i];   // bucket starts
+    for (int i = BPT - 1; i >= 0; --i) {   // bucket starts, top bucket first
+        cur[lo + i] = run;
+        run += v[i];
+    }
     __syncthreads();
     for (int i = tid; i < n; i += THREADS) {
         const uint64_t x = a[i];
-        const uint32_t pos = atomicAdd(&cur[((uint32_t)(x >> 32) - mn) >> s], 1u);
+        const uint32_t pos = atomicAdd(&cur[((uint32_t)(x >> 32) - kmin) >> s], 1u);
         b[pos] = x;
     }
     __syncthreads();
@@ -439,14 +443,15 @@ __device__ void bucket_sort_desc(uint64_t *a, uint64_t *b, int n, int cap_pow2, 
     // end of bucket d + 1 (buckets are laid out from the top digit down).
     for (int p = tid; p < n; p += THREADS) {
         const uint64_t x = b[p];
-        const uint32_t d = ((uint32_t)(x >> 32) - mn) >> s;
+        const uint32_t d = ((uint32_t)(x >> 32) - kmin) >> s;
         const uint32_t st = d + 1 < (uint32_t)kBins ? cur[d + 1] : 0u;
         const uint32_t en = cur[d];
         uint32_t rank = 0;
         for (uint32_t q = st; q < en; ++q) rank += b[q] > x;
-        a[st + rank] = x;
+        const uint32_t pos = st + rank;
+        oi[pos] = (int32_t)(idx_offset + (int32_t)(~(uint32_t)x));
+        if (ov) ov[pos] = __uint_as_float(key_bits((uint32_t)(x >> 32)));
     }
-    __syncthreads();
 }
 
 __device__ __forceinline__ void pad_out(int32_t *oi, float *ov, int from, int to)
@@ -457,15 +462,32 @@ __device__ __forceinline__ void pad_out(int32_t *oi, float *ov, int from, int to
     }
 }
 
-// ------------------------------------------------------------------------- //
-// The kernel: one row per cluster (CLUSTER) or per CTA.
-// ------------------------------------------------------------------------- //
-template <int THREADS, bool CLUSTER>
-__global__ void __launch_bounds__(THREADS, CLUSTER ? 2048 / THREADS / 2 : 2048 / THREADS / 2)
-topk_ragged_kernel(const Params p)
+// Quads of warp `warp`'s contiguous segment of the slice.
+struct WarpSeg {
+    int q0, q1;
+};
+
+template <int THREADS>
+__device__ __forceinline__ WarpSeg warp_segment(int nq, int warp)
 {
     constexpr int NW = THREADS / 32;
-    constexpr int U = 4;                       // quads in flight per lane in the streaming pass
+    const int per = (nq + NW - 1) / NW;
+    const int q0 = min(nq, warp * per);
+    return {q0, min(nq, q0 + per)};
+}
+
+// ------------------------------------------------------------------------- //
+// The kernel: one row per cluster (CLUSTER) or per CTA.
+//
+// Every pass over a CTA's slice walks the same contiguous per-warp
+// segments, U quads per lane in flight, so per-warp counts taken in one pass
+// give index-ordered positions in a later one.
+// ------------------------------------------------------------------------- //
+template <int THREADS, bool CLUSTER>
+__global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kernel(const Params p)
+{
+    constexpr int NW = THREADS / 32;
+    constexpr int U = 4;                       // quads in flight per lane
     constexpr uint32_t kZeroKey = 0x80000000u; // order key of +0.0
     constexpr uint32_t kZeroDigit = kZeroKey >> 21;
     extern __shared__ __align__(16) unsigned char smem[];
@@ -501,6 +523,7 @@ topk_ragged_kernel(const Params p)
     }
     const int32_t L = (int32_t)len;
     const uint32_t k_eff = (uint32_t)(p.k < L ? p.k : L);
+    const int64_t idx_offset = p.offset_mode == TOPK_OFFSET_ROW_START ? rs : 0;
 
     // ---- slice of this CTA (16-byte aligned body split by quads) ----------- //
     Slice s;
@@ -524,6 +547,7 @@ topk_ragged_kernel(const Params p)
         s.sq = s.nq < (p.stage_cap >> 2) ? s.nq : (p.stage_cap >> 2);
         s.jbase = (int32_t)(sbase - rs);
     }
+    const WarpSeg seg = warp_segment<THREADS>(s.nq, warp);
 
     // ---- init shared state ------------------------------------------------ //
     for (int b = tid; b < kBins; b += THREADS) {
@@ -538,32 +562,49 @@ topk_ragged_kernel(const Params p)
         ctrl.zeros = 0u;
         ctrl.zeros_tot = 0u;
         ctrl.win_count = 0u;
+        ctrl.kmax = 0u;
+        ctrl.kmax_tot = 0u;
+        ctrl.wmin = kFull;
     }
     __syncthreads();
     if (CLUSTER) cluster_arrive();   // B0: every CTA started and zeroed (waited before the flush)
 
     // ---- a2+a3: stream the slice once: key transform, stage, top-digit
-    //      histogram, and a count of exact +0.0 (the ReLU plateau) --------- //
-    uint32_t zeros = 0;
-    for (int qb = warp * 32 * U; qb < s.nq; qb += THREADS * U) {
-        uint4 kk[U];
-        uint32_t m[U];
+    //      histogram, the largest key and per-warp counts of exact +0.0 --- //
+    {
+        uint32_t zeros = 0, kmax = 0;
+        for (int qb = seg.q0; qb < seg.q1; qb += 32 * U) {
+            uint4 kk[U];
+            uint32_t m[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) kk[u] = load_quad_global(s, qb + u * 32 + lane, m[u]);
+            for (int u = 0; u < U; ++u) {
+                const int q = qb + u * 32 + lane;
+                m[u] = 0;
+                kk[u] = make_uint4(0, 0, 0, 0);
+                if (q < seg.q1) kk[u] = load_quad_global(s, q, m[u]);
+            }
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int q = qb + u * 32 + lane;
-            if (q < s.sq) reinterpret_cast<uint4 *>(keys)[q] = kk[u];
-            zeros += ((m[u] & 1u) && kk[u].x == kZeroKey) + ((m[u] & 2u) && kk[u].y == kZeroKey) +
-                     ((m[u] & 4u) && kk[u].z == kZeroKey) + ((m[u] & 8u) && kk[u].w == kZeroKey);
-            hist_add(hist, kk[u].x >> 21, m[u] & 1u);
-            hist_add(hist, kk[u].y >> 21, m[u] & 2u);
-            hist_add(hist, kk[u].z >> 21, m[u] & 4u);
-            hist_add(hist, kk[u].w >> 21, m[u] & 8u);
+            for (int u = 0; u < U; ++u) {
+                const int q = qb + u * 32 + lane;
+                if (q < s.sq && q < seg.q1) reinterpret_cast<uint4 *>(keys)[q] = kk[u];
+                const uint32_t e[4] = {kk[u].x, kk[u].y, kk[u].z, kk[u].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const bool v = (m[u] >> i) & 1u;
+                    zeros += v && e[i] == kZeroKey;
+                    kmax = max(kmax, v ? e[i] : 0u);
+                    hist_add(hist, e[i] >> 21, v);
+                }
+            }
+        }
+        zeros = __reduce_add_sync(kFull, zeros);
+        kmax = __reduce_max_sync(kFull, kmax);
+        if (lane == 0) {
+            ctrl.warp_zeros[warp] = zeros;
+            if (zeros) atomicAdd(&ctrl.zeros, zeros);
+            atomicMax(&ctrl.kmax, kmax);
         }
     }
-    zeros = __reduce_add_sync(kFull, zeros);
-    if (lane == 0 && zeros) atomicAdd(&ctrl.zeros, zeros);
     __syncthreads();
 
     const uint32_t lead_hist_tot = CLUSTER ? dsmem_addr(hist_tot, 0) : 0u;
@@ -580,14 +621,24 @@ topk_ragged_kernel(const Params p)
             const int pshift = level == 1 ? 21 : 10;
             const int dshift = level == 1 ? 10 : 0;
             const uint32_t dmask = (1u << dbits) - 1u;
-            for (int qb = warp * 32; qb < s.nq; qb += THREADS) {
-                uint32_t m;
-                const uint4 kk = load_quad(s, keys, qb + lane, m);
-                const uint32_t e[4] = {kk.x, kk.y, kk.z, kk.w};
+            for (int qb = seg.q0; qb < seg.q1; qb += 32 * U) {
+                uint4 kk[U];
+                uint32_t m[U];
 #pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const bool v = ((m >> i) & 1u) && (e[i] >> pshift) == prefix;
-                    hist_add(hist, (e[i] >> dshift) & dmask, v);
+                for (int u = 0; u < U; ++u) {
+                    const int q = qb + u * 32 + lane;
+                    m[u] = 0;
+                    kk[u] = make_uint4(0, 0, 0, 0);
+                    if (q < seg.q1) kk[u] = load_quad(s, keys, q, m[u]);
+                }
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const uint32_t e[4] = {kk[u].x, kk[u].y, kk[u].z, kk[u].w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const bool v = ((m[u] >> i) & 1u) && (e[i] >> pshift) == prefix;
+                        hist_add(hist, (e[i] >> dshift) & dmask, v);
+                    }
                 }
             }
             __syncthreads();
@@ -600,8 +651,10 @@ topk_ragged_kernel(const Params p)
                 const uint32_t v = hist[b];
                 if (v) dsmem_red_add(lead_hist_tot + 4u * (uint32_t)b, v);
             }
-            if (level == 0 && tid == 0 && ctrl.zeros)
-                dsmem_red_add(dsmem_addr(&ctrl.zeros_tot, 0), ctrl.zeros);
+            if (level == 0 && tid == 0) {
+                if (ctrl.zeros) dsmem_red_add(dsmem_addr(&ctrl.zeros_tot, 0), ctrl.zeros);
+                dsmem_red_max(dsmem_addr(&ctrl.kmax_tot, 0), ctrl.kmax);
+            }
             cluster_sync();   // B1: the leader holds the cluster-wide histogram
             htot = hist_tot;
         }
@@ -661,10 +714,15 @@ topk_ragged_kernel(const Params p)
         __syncthreads();
     }
     const uint32_t T = prefix;   // exact k-th key; n_gt above it, take r of its cnt ties
+    const uint32_t tval = key_bits(T);
 
-    // ---- a6: winners (key > T) go to the leader's list in any order (their
-    //      composites are unique, the sort makes the order canonical); ties
-    //      (key == T) are counted per warp over contiguous warp segments. --- //
+    // ---- a6+a7: one pass over the slice.  Winners (key > T) go to the
+    //      leader's list in any order (their composites are unique, the sort
+    //      makes the order canonical).  Ties (key == T): the first r in
+    //      cluster-wide index order go straight to positions n_gt + ordinal.
+    //      On the plateau every tie is a +0.0 and the per-warp zero counts of
+    //      the streaming pass already give each warp's first ordinal; else
+    //      the pass counts ties per warp and a second pass writes them. --- //
     uint32_t tie_base = 0, local_eq = cnt;
     if (CLUSTER) {
         local_eq = plateau ? ctrl.zeros : hist[T & 0x3FFu];
@@ -677,57 +735,104 @@ topk_ragged_kernel(const Params p)
         if (tid == 0) ctrl.scan[0] = part;
         __syncthreads();
         tie_base = ctrl.scan[0];
-        __syncthreads();
     }
     const bool want_ties = local_eq > 0 && tie_base < r;   // CTA-uniform
+    uint32_t trun = 0;   // this warp's next tie ordinal (plateau)
+    if (plateau && want_ties) {
+        if (warp == 0) {
+            const uint32_t z = lane < NW ? ctrl.warp_zeros[lane] : 0u;
+            const uint32_t zi = warp_incl_scan(z);
+            if (lane < NW) ctrl.warp_ties[lane] = zi - z;
+        }
+        __syncthreads();
+        trun = tie_base + ctrl.warp_ties[warp];
+    }
+    const bool fused_ties = plateau && want_ties && ctrl.warp_zeros[warp] > 0;   // warp-uniform
     const uint32_t win_count_addr = CLUSTER ? dsmem_addr(&ctrl.win_count, 0) : 0u;
     const uint32_t win_addr = CLUSTER ? dsmem_addr(win, 0) : 0u;
-    const int per_warp = (s.nq + NW - 1) / NW;
-    const int wq0 = warp * per_warp;
-    const int wq1 = (wq0 + per_warp) < s.nq ? (wq0 + per_warp) : s.nq;
-    uint32_t ties_w = 0;
-    for (int qb = wq0; qb < wq1; qb += 32) {
-        const int q = qb + lane;
-        uint32_t m = 0;
-        uint4 kk = make_uint4(0, 0, 0, 0);
-        if (q < wq1) kk = load_quad(s, keys, q, m);
-        const uint32_t e[4] = {kk.x, kk.y, kk.z, kk.w};
-        uint32_t wm = 0, tc = 0;
+    uint32_t ties_w = 0, wmin = kFull;
+    int first_tie_q = seg.q1;
+    for (int qb = seg.q0; qb < seg.q1; qb += 32 * U) {
+        uint4 kk[U];
+        uint32_t m[U];
 #pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const bool v = (m >> i) & 1u;
-            if (v && e[i] > T) wm |= 1u << i;
-            tc += v && e[i] == T;
+        for (int u = 0; u < U; ++u) {
+            const int q = qb + u * 32 + lane;
+            m[u] = 0;
+            kk[u] = make_uint4(0, 0, 0, 0);
+            if (q < seg.q1) kk[u] = load_quad(s, keys, q, m[u]);
         }
-        if (want_ties) ties_w += __reduce_add_sync(kFull, tc);
-        const uint32_t wc = (uint32_t)__popc(wm);
-        const uint32_t any = __ballot_sync(kFull, wc != 0);
-        if (any) {
-            const uint32_t wincl = warp_incl_scan(wc);
-            const uint32_t wtot = __shfl_sync(kFull, wincl, 31);
-            uint32_t base = 0;
-            if (lane == 31)
-                base = CLUSTER ? dsmem_atom_add(win_count_addr, wtot) : atomicAdd(&ctrl.win_count, wtot);
-            base = __shfl_sync(kFull, base, 31);
-            uint32_t slot = base + wincl - wc;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int q = qb + u * 32 + lane;
+            const uint32_t e[4] = {kk[u].x, kk[u].y, kk[u].z, kk[u].w};
+            uint32_t wm = 0, tm = 0;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                if ((wm >> i) & 1u) {
-                    const uint32_t j = (uint32_t)(s.jbase + 4 * q + i);
-                    const uint64_t comp = ((uint64_t)e[i] << 32) | (uint64_t)(~j);
-                    if (slot < (uint32_t)p.win_cap) {
-                        if (CLUSTER) dsmem_st64(win_addr + 8u * slot, comp);
-                        else win[slot] = comp;
+                if ((m[u] >> i) & 1u) {
+                    if (e[i] > T) wm |= 1u << i;
+                    else if (e[i] == T) tm |= 1u << i;
+                }
+            }
+            const uint32_t wc = (uint32_t)__popc(wm), tc = (uint32_t)__popc(tm);
+            if (__ballot_sync(kFull, wc != 0)) {
+                const uint32_t wincl = warp_incl_scan(wc);
+                uint32_t base = 0;
+                if (lane == 31)
+                    base = CLUSTER ? dsmem_atom_add(win_count_addr, wincl) : atomicAdd(&ctrl.win_count, wincl);
+                base = __shfl_sync(kFull, base, 31);
+                uint32_t slot = base + wincl - wc;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    if ((wm >> i) & 1u) {
+                        const uint32_t j = (uint32_t)(s.jbase + 4 * q + i);
+                        const uint64_t comp = ((uint64_t)e[i] << 32) | (uint64_t)(~j);
+                        wmin = min(wmin, e[i]);
+                        if (slot < (uint32_t)p.win_cap) {
+                            if (CLUSTER) dsmem_st64(win_addr + 8u * slot, comp);
+                            else win[slot] = comp;
+                        }
+                        ++slot;
                     }
-                    ++slot;
+                }
+            }
+            const uint32_t tb = __ballot_sync(kFull, tc != 0);
+            if (tb) {
+                if (fused_ties) {
+                    if (trun < r) {
+                        const uint32_t tincl = warp_incl_scan(tc);
+                        uint32_t tord = trun + tincl - tc;
+#pragma unroll
+                        for (int i = 0; i < 4; ++i) {
+                            if ((tm >> i) & 1u) {
+                                if (tord < r && n_gt + tord < k_eff) {
+                                    const int32_t j = s.jbase + 4 * q + i;
+                                    oi[n_gt + tord] = (int32_t)(idx_offset + j);
+                                    if (ov) ov[n_gt + tord] = __uint_as_float(tval);
+                                }
+                                ++tord;
+                            }
+                        }
+                        trun += __shfl_sync(kFull, tincl, 31);
+                    }
+                } else if (want_ties) {
+                    ties_w += __reduce_add_sync(kFull, tc);
+                    const int fq = qb + u * 32 + __ffs(tb) - 1;
+                    if (fq < first_tie_q) first_tie_q = fq;
                 }
             }
         }
     }
 
-    // ---- a7: the first r ties in cluster-wide index order go to positions
-    //      n_gt + ordinal (their canonical place, right after the winners) -- //
-    if (want_ties) {
+    wmin = __reduce_min_sync(kFull, wmin);
+    if (lane == 0 && wmin != kFull) {
+        if (CLUSTER) dsmem_red_min(dsmem_addr(&ctrl.wmin, 0), wmin);
+        else atomicMin(&ctrl.wmin, wmin);
+    }
+
+    // ---- a7 (off the plateau): ties in index order, per-warp bases from
+    //      the counts above; each warp starts at its first tie ------------ //
+    if (want_ties && !plateau) {
         if (lane == 0) ctrl.warp_ties[warp] = ties_w;
         __syncthreads();
         if (warp == 0) {
@@ -736,22 +841,20 @@ topk_ragged_kernel(const Params p)
             if (lane < NW) ctrl.warp_ties[lane] = bi - b;
         }
         __syncthreads();
-        uint32_t trun = tie_base + ctrl.warp_ties[warp];
-        const uint32_t tval = key_bits(T);
+        trun = tie_base + ctrl.warp_ties[warp];
         if (ties_w > 0 && trun < r) {   // warp-uniform
-            for (int qb = wq0; qb < wq1 && trun < r; qb += 32) {
+            for (int qb = first_tie_q; qb < seg.q1 && trun < r; qb += 32) {
                 const int q = qb + lane;
                 uint32_t m = 0;
                 uint4 kk = make_uint4(0, 0, 0, 0);
-                if (q < wq1) kk = load_quad(s, keys, q, m);
+                if (q < seg.q1) kk = load_quad(s, keys, q, m);
                 const uint32_t e[4] = {kk.x, kk.y, kk.z, kk.w};
                 uint32_t tm = 0;
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     if (((m >> i) & 1u) && e[i] == T) tm |= 1u << i;
                 const uint32_t tc = (uint32_t)__popc(tm);
-                const uint32_t tb = __ballot_sync(kFull, tc != 0);
-                if (tb) {
+                if (__ballot_sync(kFull, tc != 0)) {
                     const uint32_t tincl = warp_incl_scan(tc);
                     uint32_t tord = trun + tincl - tc;
 #pragma unroll
@@ -759,9 +862,8 @@ topk_ragged_kernel(const Params p)
                         if ((tm >> i) & 1u) {
                             if (tord < r && n_gt + tord < k_eff) {
                                 const int32_t j = s.jbase + 4 * q + i;
-                                const uint32_t pos = n_gt + tord;
-                                oi[pos] = p.offset_mode == TOPK_OFFSET_ROW_START ? (int32_t)(rs + j) : j;
-                                if (ov) ov[pos] = __uint_as_float(tval);
+                                oi[n_gt + tord] = (int32_t)(idx_offset + j);
+                                if (ov) ov[n_gt + tord] = __uint_as_float(tval);
                             }
                             ++tord;
                         }
@@ -785,14 +887,9 @@ topk_ragged_kernel(const Params p)
     }
     const uint32_t n_sort = n_gt < (uint32_t)p.win_cap ? n_gt : (uint32_t)p.win_cap;
     if (n_sort > 0) {
-        bucket_sort_desc<THREADS>(win, reinterpret_cast<uint64_t *>(keys), (int)n_sort, p.win_cap,
-                                  hist, ctrl.scan, ctrl.red);
-        for (uint32_t pidx = tid; pidx < n_sort; pidx += THREADS) {
-            const uint64_t c = win[pidx];
-            const int32_t j = (int32_t)(~(uint32_t)c);
-            oi[pidx] = p.offset_mode == TOPK_OFFSET_ROW_START ? (int32_t)(rs + j) : j;
-            if (ov) ov[pidx] = __uint_as_float(key_bits((uint32_t)(c >> 32)));
-        }
+        const uint32_t kmax = CLUSTER ? ctrl.kmax_tot : ctrl.kmax;
+        sort_and_write<THREADS>(win, reinterpret_cast<uint64_t *>(keys), (int)n_sort, p.win_cap,
+                                ctrl.wmin, kmax, hist, ctrl.scan64, oi, ov, idx_offset);
     }
     pad_out(oi, ov, (int)k_eff, p.k);
 }
