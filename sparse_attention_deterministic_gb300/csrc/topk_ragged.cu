@@ -59,6 +59,7 @@ struct Params {
     int32_t win_cap;     // winner slots in the leader (power of two >= k - 1)
     int32_t off_win;     // byte offset of the winner array in dynamic smem
     int32_t off_keys;    // byte offset of the staged keys in dynamic smem
+    int32_t grouped;     // clusters take groups of rows (see assign_rows)
 };
 
 // Per-CTA control block at the start of dynamic shared memory.
@@ -323,6 +324,13 @@ __device__ __forceinline__ bool find_bin(const uint32_t *h, uint32_t r, uint32_t
     return mine;
 }
 
+__device__ __forceinline__ uint32_t lanemask_lt()
+{
+    uint32_t m;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(m));
+    return m;
+}
+
 // ------------------------------------------------------------------------- //
 // Descending bitonic sort of n = power of two composites (the fallback of
 // bucket_sort_desc for pathologically skewed key distributions).
@@ -476,8 +484,123 @@ __device__ __forceinline__ WarpSeg warp_segment(int nq, int warp)
     return {q0, min(nq, q0 + per)};
 }
 
+// Row assignment of a grouped cluster: every CTA of the cluster computes it
+// from the row lengths alone, so all of them agree.  Rows are ranked by
+// valid length (descending, index ascending); rank t goes to cluster
+// snake(t) (0..G-1, then G-1..0, ...), which spreads long rows over the
+// clusters; inside a cluster the CTAs are dealt to its rows in proportion to
+// their lengths (at least one each), so every CTA gets a similar slice.
+struct RowGroup {
+    int row;        // my row, or -1 when the cluster has no row with work
+    uint32_t g0;    // cluster rank of the group's first CTA (its leader)
+    uint32_t gsize; // CTAs working on the row
+};
+
+__device__ __forceinline__ bool row_window_ok(const Params &p, int i, int64_t &len)
+{
+    const int64_t rs = p.row_starts[i];
+    len = p.lengths[i];
+    if (len < 0) len = 0;
+    if (len >= (int64_t)TOPK_RAGGED_MAX_LEN) return false;
+    return rs >= 0 && rs + len <= p.n_scores;
+}
+
+template <int THREADS>
+__device__ RowGroup assign_rows(const Params &p, uint32_t crank, uint32_t csize, uint32_t *scratch,
+                                uint32_t *slot)
+{
+    const int tid = threadIdx.x;
+    const int B = p.B;
+    const int G = (int)(gridDim.x / csize), cid = (int)(blockIdx.x / csize);
+    uint32_t *eff = scratch;              // B valid lengths (0: nothing to select)
+    uint32_t *by_rank = scratch + 1024;   // row index of every rank
+    for (int i = tid; i < B; i += THREADS) {
+        int64_t len;
+        eff[i] = row_window_ok(p, i, len) ? (uint32_t)len : 0u;
+    }
+    __syncthreads();
+    for (int i = tid; i < B; i += THREADS) {
+        const uint32_t e = eff[i];
+        int rank = 0;
+        for (int j = 0; j < B; ++j) {
+            const uint32_t ej = eff[j];
+            rank += (ej > e) || (ej == e && j < i);
+        }
+        by_rank[rank] = (uint32_t)i;
+    }
+    __syncthreads();
+    if (tid == 0) {
+        int rows[16];
+        uint32_t len[16];
+        int m = 0;
+        for (int t0 = 0; t0 < B; t0 += 2 * G) {
+            const int ta = t0 + cid, tb = t0 + 2 * G - 1 - cid;
+            if (ta < B && m < 16) { rows[m] = (int)by_rank[ta]; len[m] = eff[rows[m]]; ++m; }
+            if (tb < B && m < 16) { rows[m] = (int)by_rank[tb]; len[m] = eff[rows[m]]; ++m; }
+        }
+        // Rows are listed in rank order, so the rows with work come first.
+        int mv = 0;
+        uint64_t E = 0;
+        while (mv < m && len[mv] > 0) E += len[mv++];
+        int mine = -1;
+        uint32_t g0 = 0, gsize = 0;
+        if (mv > 0) {
+            uint32_t c[16];
+            uint32_t used = 0;
+            const uint32_t spare = csize - (uint32_t)mv;
+            for (int i = 0; i < mv; ++i) {
+                c[i] = 1u + (uint32_t)((uint64_t)spare * len[i] / E);
+                used += c[i];
+            }
+            for (int i = 0; used < csize; i = (i + 1) % mv) {
+                ++c[i];
+                ++used;
+            }
+            uint32_t start = 0;
+            for (int i = 0; i < mv; ++i) {
+                if (crank >= start && crank < start + c[i]) {
+                    mine = rows[i];
+                    g0 = start;
+                    gsize = c[i];
+                }
+                start += c[i];
+            }
+        }
+        slot[0] = (uint32_t)mine;
+        slot[1] = g0;
+        slot[2] = gsize;
+        // The cluster's first CTA pads the rows with nothing to select.
+        slot[3] = (uint32_t)(m - mv);
+        for (int i = mv; i < m; ++i) slot[4 + i - mv] = (uint32_t)rows[i];
+    }
+    __syncthreads();
+    RowGroup g;
+    g.row = (int)slot[0];
+    g.g0 = slot[1];
+    g.gsize = slot[2];
+    if (crank == 0) {
+        const int npad = (int)slot[3];
+        for (int i = 0; i < npad; ++i) {
+            const int rr = (int)slot[4 + i];
+            int64_t len;
+            const bool ok = row_window_ok(p, rr, len);
+            if (!ok && tid == 0)
+                atomicOr(&g_status, len >= (int64_t)TOPK_RAGGED_MAX_LEN ? TOPK_DEV_LEN_ENVELOPE
+                                                                         : TOPK_DEV_BAD_WINDOW);
+            pad_out(p.out_idx + (int64_t)rr * p.k, p.out_val ? p.out_val + (int64_t)rr * p.k : nullptr,
+                    0, p.k);
+        }
+    }
+    __syncthreads();
+    return g;
+}
+
 // ------------------------------------------------------------------------- //
-// The kernel: one row per cluster (CLUSTER) or per CTA.
+// The kernel.  CLUSTER = false: one row per CTA.  CLUSTER = true: each
+// cluster takes a group of rows (assign_rows) and every row is worked on by
+// a contiguous group of the cluster's CTAs; the group's first CTA is the
+// row's leader (cluster-wide histograms, threshold search, winner list,
+// sort).  With one row per cluster the group is the whole cluster.
 //
 // Every pass over a CTA's slice walks the same contiguous per-warp
 // segments, U quads per lane in flight, so per-warp counts taken in one pass
@@ -493,15 +616,31 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
     extern __shared__ __align__(16) unsigned char smem[];
     Ctrl &ctrl = *reinterpret_cast<Ctrl *>(smem);
     uint32_t *hist = reinterpret_cast<uint32_t *>(smem + sizeof(Ctrl));
-    uint32_t *hist_tot = hist + kBins;   // leader's cluster-wide histogram (CLUSTER only)
+    uint32_t *hist_tot = hist + kBins;   // the row leader's group-wide histogram (CLUSTER only)
     uint64_t *win = reinterpret_cast<uint64_t *>(smem + p.off_win);
     uint32_t *keys = reinterpret_cast<uint32_t *>(smem + p.off_keys);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const uint32_t crank = CLUSTER ? cluster_rank() : 0u;
-    const uint32_t csize = CLUSTER ? cluster_size() : 1u;
-    const int row = (int)(blockIdx.x / csize);
-    const bool leader = crank == 0;
+    int row;
+    uint32_t grank = 0, gsize = 1, g0 = 0;
+    if (CLUSTER) {
+        const uint32_t crank = cluster_rank(), csize = cluster_size();
+        if (p.grouped) {
+            const RowGroup g = assign_rows<THREADS>(p, crank, csize, hist, ctrl.scan);
+            if (g.row < 0) return;   // uniform over the cluster: nothing to select
+            row = g.row;
+            g0 = g.g0;
+            gsize = g.gsize;
+            grank = crank - g0;
+        } else {
+            row = (int)(blockIdx.x / csize);
+            gsize = csize;
+            grank = crank;
+        }
+    } else {
+        row = (int)blockIdx.x;
+    }
+    const bool leader = grank == 0;
 
     // ---- a1: metadata, window checks ----------------------------------- //
     const int64_t rs = p.row_starts[row];
@@ -515,11 +654,14 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
     int32_t *oi = p.out_idx + (int64_t)row * p.k;
     float *ov = p.out_val ? p.out_val + (int64_t)row * p.k : nullptr;
     if (bad || len == 0) {
+        // Grouped clusters never get here (such rows are padded above); with
+        // one row per cluster the decision is uniform over the cluster and
+        // precedes every cluster barrier.
         if (leader) {
             if (bad && tid == 0) atomicOr(&g_status, bad);
             pad_out(oi, ov, 0, p.k);
         }
-        return;   // uniform over the cluster: no barrier has been used yet
+        return;
     }
     const int32_t L = (int32_t)len;
     const uint32_t k_eff = (uint32_t)(p.k < L ? p.k : L);
@@ -529,14 +671,14 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
     Slice s;
     {
         const uint64_t pa = (uint64_t)(uintptr_t)p.scores >> 2;   // element address
-        const int64_t g0 = rs, g1 = rs + L;
-        int64_t a0 = g0 + (int64_t)((4u - (uint32_t)((pa + (uint64_t)g0) & 3u)) & 3u);
-        if (a0 > g1) a0 = g1;
-        const int64_t n4 = (g1 - a0) >> 2;
-        const int64_t qlo = n4 * crank / csize, qhi = n4 * (crank + 1) / csize;
+        const int64_t e0 = rs, e1 = rs + L;
+        int64_t a0 = e0 + (int64_t)((4u - (uint32_t)((pa + (uint64_t)e0) & 3u)) & 3u);
+        if (a0 > e1) a0 = e1;
+        const int64_t n4 = (e1 - a0) >> 2;
+        const int64_t qlo = n4 * grank / gsize, qhi = n4 * (grank + 1) / gsize;
         const int64_t hb = a0 + 4 * qlo, he = a0 + 4 * qhi;
-        const int64_t glo = crank == 0 ? g0 : hb;
-        const int64_t ghi = crank == csize - 1 ? g1 : he;
+        const int64_t glo = grank == 0 ? e0 : hb;
+        const int64_t ghi = grank == gsize - 1 ? e1 : he;
         const int64_t sbase = hb - ((hb - glo + 3) & ~(int64_t)3);
         s.gptr = p.scores + sbase;
         s.off0 = (int32_t)(glo - sbase);
@@ -585,6 +727,7 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
             }
 #pragma unroll
             for (int u = 0; u < U; ++u) {
+                if (qb + u * 32 >= seg.q1) break;   // warp-uniform
                 const int q = qb + u * 32 + lane;
                 if (q < s.sq && q < seg.q1) reinterpret_cast<uint4 *>(keys)[q] = kk[u];
                 const uint32_t e[4] = {kk[u].x, kk[u].y, kk[u].z, kk[u].w};
@@ -607,17 +750,20 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
     }
     __syncthreads();
 
-    const uint32_t lead_hist_tot = CLUSTER ? dsmem_addr(hist_tot, 0) : 0u;
+    const uint32_t lead_hist_tot = CLUSTER ? dsmem_addr(hist_tot, g0) : 0u;
 
-    // Running selection state (identical in every thread of the cluster).
+    // Running selection state (identical in every thread of the group).
     uint32_t prefix = 0, n_gt = 0, r = k_eff, cnt = 0;
     bool plateau = false;   // T is +0.0, found from the zero count
+    bool sel_done = false;  // the k-th key is known
 
-    // ---- a4+a5: radix levels of 11, 11 and 10 bits ------------------------ //
+    // ---- a4+a5: radix levels of 11, 11 and 10 bits.  In a cluster every
+    //      CTA runs all three levels' barriers, working or not, because the
+    //      cluster's rows may finish at different levels. --------------- //
 #pragma unroll 1
     for (int level = 0; level < 3; ++level) {
         const int dbits = level == 2 ? 10 : 11;
-        if (level > 0) {
+        if (level > 0 && !sel_done) {
             const int pshift = level == 1 ? 21 : 10;
             const int dshift = level == 1 ? 10 : 0;
             const uint32_t dmask = (1u << dbits) - 1u;
@@ -633,6 +779,7 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
                 }
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
+                    if (qb + u * 32 >= seg.q1) break;   // warp-uniform
                     const uint32_t e[4] = {kk[u].x, kk[u].y, kk[u].z, kk[u].w};
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
@@ -646,26 +793,28 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
         uint32_t d = 0, gt = 0, c = 0;
         const uint32_t *htot = hist;
         if (CLUSTER) {
-            if (level == 0) cluster_wait();   // B0 complete: the leader's totals are zeroed
-            for (int b = tid; b < kBins; b += THREADS) {
-                const uint32_t v = hist[b];
-                if (v) dsmem_red_add(lead_hist_tot + 4u * (uint32_t)b, v);
+            if (level == 0) cluster_wait();   // B0 complete: the leaders' totals are zeroed
+            if (!sel_done) {
+                for (int b = tid; b < kBins; b += THREADS) {
+                    const uint32_t v = hist[b];
+                    if (v) dsmem_red_add(lead_hist_tot + 4u * (uint32_t)b, v);
+                }
+                if (level == 0 && tid == 0) {
+                    if (ctrl.zeros) dsmem_red_add(dsmem_addr(&ctrl.zeros_tot, g0), ctrl.zeros);
+                    dsmem_red_max(dsmem_addr(&ctrl.kmax_tot, g0), ctrl.kmax);
+                }
             }
-            if (level == 0 && tid == 0) {
-                if (ctrl.zeros) dsmem_red_add(dsmem_addr(&ctrl.zeros_tot, 0), ctrl.zeros);
-                dsmem_red_max(dsmem_addr(&ctrl.kmax_tot, 0), ctrl.kmax);
-            }
-            cluster_sync();   // B1: the leader holds the cluster-wide histogram
+            cluster_sync();   // B1: each leader holds its group's histogram
             htot = hist_tot;
         }
-        if (!CLUSTER || leader) {
+        if ((!CLUSTER || leader) && !sel_done) {
             if (find_bin<THREADS>(htot, r, ctrl.scan, d, gt, c)) {
                 // Plateau shortcut: the boundary bin holds only exact +0.0, so
                 // the k-th key is +0.0 and the finer levels are not needed.
                 const uint32_t ztot = CLUSTER ? ctrl.zeros_tot : ctrl.zeros;
                 const uint32_t done = (level == 0 && d == kZeroDigit && c == ztot) ? 1u : 0u;
                 if (CLUSTER) {
-                    for (uint32_t rk = 0; rk < csize; ++rk) {
+                    for (uint32_t rk = g0; rk < g0 + gsize; ++rk) {
                         dsmem_st(dsmem_addr(&ctrl.sel_digit, rk), d);
                         dsmem_st(dsmem_addr(&ctrl.sel_gt, rk), gt);
                         dsmem_st(dsmem_addr(&ctrl.sel_cnt, rk), c);
@@ -680,38 +829,42 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
             }
         }
         if (CLUSTER) {
-            if (leader) {
+            if (leader && !sel_done) {
                 __syncthreads();
                 for (int b = tid; b < kBins; b += THREADS) hist_tot[b] = 0u;
             }
-            cluster_sync();   // B2: selection visible everywhere
+            cluster_sync();   // B2: selections visible to every CTA of their group
         } else {
             __syncthreads();
         }
-        d = ctrl.sel_digit;
-        gt = ctrl.sel_gt;
-        c = ctrl.sel_cnt;
-        const bool done = ctrl.sel_done != 0u;
-        // Exact integer counts guarantee gt < r <= gt + c; anything else is a
-        // library bug: flag it and keep every later write inside the row.
-        if (gt >= r || r - gt > c) {
-            if (tid == 0) atomicOr(&g_status, TOPK_DEV_INTERNAL);
-            gt = r - 1u;
-            c = 1u;
+        if (!sel_done) {
+            d = ctrl.sel_digit;
+            gt = ctrl.sel_gt;
+            c = ctrl.sel_cnt;
+            const bool done = ctrl.sel_done != 0u;
+            // Exact integer counts guarantee gt < r <= gt + c; anything else
+            // is a library bug: flag it and keep every later write in the row.
+            if (gt >= r || r - gt > c) {
+                if (tid == 0) atomicOr(&g_status, TOPK_DEV_INTERNAL);
+                gt = r - 1u;
+                c = 1u;
+            }
+            n_gt += gt;
+            r -= gt;
+            cnt = c;
+            if (done) {
+                prefix = kZeroKey;
+                plateau = true;
+                sel_done = true;
+            } else {
+                prefix = (prefix << dbits) | d;
+                if (level == 2) sel_done = true;
+                else
+                    for (int b = tid; b < kBins; b += THREADS) hist[b] = 0u;
+            }
         }
-        n_gt += gt;
-        r -= gt;
-        cnt = c;
-        if (done) {
-            prefix = kZeroKey;
-            plateau = true;
-            __syncthreads();
-            break;
-        }
-        prefix = (prefix << dbits) | d;
-        if (level < 2)
-            for (int b = tid; b < kBins; b += THREADS) hist[b] = 0u;
         __syncthreads();
+        if (!CLUSTER && sel_done) break;
     }
     const uint32_t T = prefix;   // exact k-th key; n_gt above it, take r of its cnt ties
     const uint32_t tval = key_bits(T);
@@ -719,7 +872,7 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
     // ---- a6+a7: one pass over the slice.  Winners (key > T) go to the
     //      leader's list in any order (their composites are unique, the sort
     //      makes the order canonical).  Ties (key == T): the first r in
-    //      cluster-wide index order go straight to positions n_gt + ordinal.
+    //      group-wide index order go straight to positions n_gt + ordinal.
     //      On the plateau every tie is a +0.0 and the per-warp zero counts of
     //      the streaming pass already give each warp's first ordinal; else
     //      the pass counts ties per warp and a second pass writes them. --- //
@@ -727,9 +880,9 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
     if (CLUSTER) {
         local_eq = plateau ? ctrl.zeros : hist[T & 0x3FFu];
         uint32_t part = 0;
-        if (warp == 0 && lane < (int)crank) {
+        if (warp == 0 && lane < (int)grank) {
             const void *src = plateau ? (const void *)&ctrl.zeros : (const void *)&hist[T & 0x3FFu];
-            part = dsmem_ld(dsmem_addr(src, (uint32_t)lane));
+            part = dsmem_ld(dsmem_addr(src, g0 + (uint32_t)lane));
         }
         if (warp == 0) part = __reduce_add_sync(kFull, part);
         if (tid == 0) ctrl.scan[0] = part;
@@ -748,10 +901,11 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
         trun = tie_base + ctrl.warp_ties[warp];
     }
     const bool fused_ties = plateau && want_ties && ctrl.warp_zeros[warp] > 0;   // warp-uniform
-    const uint32_t win_count_addr = CLUSTER ? dsmem_addr(&ctrl.win_count, 0) : 0u;
-    const uint32_t win_addr = CLUSTER ? dsmem_addr(win, 0) : 0u;
+    const uint32_t win_count_addr = CLUSTER ? dsmem_addr(&ctrl.win_count, g0) : 0u;
+    const uint32_t win_addr = CLUSTER ? dsmem_addr(win, g0) : 0u;
     uint32_t ties_w = 0, wmin = kFull;
     int first_tie_q = seg.q1;
+    const uint32_t lt = lanemask_lt();
     for (int qb = seg.q0; qb < seg.q1; qb += 32 * U) {
         uint4 kk[U];
         uint32_t m[U];
@@ -764,6 +918,7 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
         }
 #pragma unroll
         for (int u = 0; u < U; ++u) {
+            if (qb + u * 32 >= seg.q1) break;   // warp-uniform
             const int q = qb + u * 32 + lane;
             const uint32_t e[4] = {kk[u].x, kk[u].y, kk[u].z, kk[u].w};
             uint32_t wm = 0, tm = 0;
@@ -774,14 +929,20 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
                     else if (e[i] == T) tm |= 1u << i;
                 }
             }
-            const uint32_t wc = (uint32_t)__popc(wm), tc = (uint32_t)__popc(tm);
-            if (__ballot_sync(kFull, wc != 0)) {
-                const uint32_t wincl = warp_incl_scan(wc);
+            // Per-slot ballots give every lane its prefix count without a
+            // shuffle scan; lane order then slot order is index order.
+            if (__ballot_sync(kFull, wm != 0)) {
+                uint32_t wtot = 0, slot = 0;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t b = __ballot_sync(kFull, (wm >> i) & 1u);
+                    wtot += (uint32_t)__popc(b);
+                    slot += (uint32_t)__popc(b & lt);
+                }
                 uint32_t base = 0;
-                if (lane == 31)
-                    base = CLUSTER ? dsmem_atom_add(win_count_addr, wincl) : atomicAdd(&ctrl.win_count, wincl);
-                base = __shfl_sync(kFull, base, 31);
-                uint32_t slot = base + wincl - wc;
+                if (lane == 0)
+                    base = CLUSTER ? dsmem_atom_add(win_count_addr, wtot) : atomicAdd(&ctrl.win_count, wtot);
+                slot += __shfl_sync(kFull, base, 0);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     if ((wm >> i) & 1u) {
@@ -796,12 +957,18 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
                     }
                 }
             }
-            const uint32_t tb = __ballot_sync(kFull, tc != 0);
-            if (tb) {
+            const uint32_t tany = __ballot_sync(kFull, tm != 0);
+            if (tany) {
+                uint32_t ttot = 0, tord = 0;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t b = __ballot_sync(kFull, (tm >> i) & 1u);
+                    ttot += (uint32_t)__popc(b);
+                    tord += (uint32_t)__popc(b & lt);
+                }
                 if (fused_ties) {
                     if (trun < r) {
-                        const uint32_t tincl = warp_incl_scan(tc);
-                        uint32_t tord = trun + tincl - tc;
+                        tord += trun;
 #pragma unroll
                         for (int i = 0; i < 4; ++i) {
                             if ((tm >> i) & 1u) {
@@ -813,20 +980,19 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
                                 ++tord;
                             }
                         }
-                        trun += __shfl_sync(kFull, tincl, 31);
                     }
+                    trun += ttot;
                 } else if (want_ties) {
-                    ties_w += __reduce_add_sync(kFull, tc);
-                    const int fq = qb + u * 32 + __ffs(tb) - 1;
+                    ties_w += ttot;
+                    const int fq = qb + u * 32 + __ffs(tany) - 1;
                     if (fq < first_tie_q) first_tie_q = fq;
                 }
             }
         }
     }
-
     wmin = __reduce_min_sync(kFull, wmin);
     if (lane == 0 && wmin != kFull) {
-        if (CLUSTER) dsmem_red_min(dsmem_addr(&ctrl.wmin, 0), wmin);
+        if (CLUSTER) dsmem_red_min(dsmem_addr(&ctrl.wmin, g0), wmin);
         else atomicMin(&ctrl.wmin, wmin);
     }
 
@@ -853,10 +1019,14 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
 #pragma unroll
                 for (int i = 0; i < 4; ++i)
                     if (((m >> i) & 1u) && e[i] == T) tm |= 1u << i;
-                const uint32_t tc = (uint32_t)__popc(tm);
-                if (__ballot_sync(kFull, tc != 0)) {
-                    const uint32_t tincl = warp_incl_scan(tc);
-                    uint32_t tord = trun + tincl - tc;
+                if (__ballot_sync(kFull, tm != 0)) {
+                    uint32_t ttot = 0, tord = trun;
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) {
+                        const uint32_t b = __ballot_sync(kFull, (tm >> i) & 1u);
+                        ttot += (uint32_t)__popc(b);
+                        tord += (uint32_t)__popc(b & lt);
+                    }
 #pragma unroll
                     for (int i = 0; i < 4; ++i) {
                         if ((tm >> i) & 1u) {
@@ -868,7 +1038,7 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
                             ++tord;
                         }
                     }
-                    trun += __shfl_sync(kFull, tincl, 31);
+                    trun += ttot;
                 }
             }
         }
@@ -876,7 +1046,7 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
 
     // ---- a8+a9: the leader sorts the winners and writes the row ----------- //
     if (CLUSTER) {
-        cluster_sync();   // B3: every winner is in the leader's list
+        cluster_sync();   // B3: every winner is in its leader's list
         if (!leader) return;
     } else {
         __syncthreads();
@@ -927,6 +1097,7 @@ DeviceInfo g_devices[kMaxDevices];
 struct Plan {
     const Variant *v;
     int cluster;
+    int grouped;
     int stage_cap;
     int win_cap;
     int off_win, off_keys, smem;
@@ -946,34 +1117,42 @@ int header_bytes(bool cluster)
 }
 
 // Launch shape from the host arguments alone (row lengths live on the
-// device and are never read here).  Large batches get one 256-thread CTA per
-// row, several CTAs per SM.  Smaller batches get a cluster of C CTAs per row,
-// C the largest power of two <= 16 that keeps the whole grid resident in one
-// wave at two 512-thread CTAs per SM; batches that fit 16-CTA clusters at one
-// CTA per SM use 1024-thread CTAs with all of an SM's shared memory, which
-// gives very long rows the most staging space.  Each CTA stages what shared
-// memory allows and re-reads the rest of its slice from L2.
+// device and are never read here).
+//   * B >= 4 x SMs: one 256-thread CTA per row, several CTAs per SM.
+//   * B x 16 <= SMs: a 16-CTA cluster of 1024-thread CTAs per row, each CTA
+//     with all of an SM's shared memory (very long rows stage the most).
+//   * otherwise: one resident wave of G clusters of CS 512-thread CTAs (two
+//     per SM); the clusters share out the rows by length and each cluster
+//     deals its CTAs to its rows in proportion to their lengths
+//     (assign_rows), so every CTA gets a similar slice.
+//   * batches too large for that wave fall back to one CTA per row.
+// Each CTA stages what shared memory allows and re-reads the rest of its
+// slice from L2.
 Plan make_plan(int32_t B, int32_t k, const DeviceInfo &dev)
 {
     Plan pl{};
     pl.win_cap = next_pow2(k - 1 > 1 ? k - 1 : 1);
     const int sms = dev.sm_count;
-    int vi, cluster, smem_budget;
-    if (B >= 4 * sms) {
-        vi = 0;
-        cluster = 1;
-        smem_budget = 0;
-    } else {
-        cluster = 1;
-        while (cluster < 16 && (int64_t)B * cluster * 2 <= 2 * (int64_t)sms &&
-               dev.max_clusters[1][cluster * 2] > 0)
-            cluster *= 2;
-        if (cluster == 16 && B * 16 <= sms && dev.max_clusters[2][16] > 0) {
+    int vi = 0, cluster = 1, smem_budget = 0, grid = B;
+    pl.grouped = 0;
+    if (B < 4 * sms) {
+        if ((int64_t)B * 16 <= sms && dev.max_clusters[2][16] > 0) {
             vi = 2;
+            cluster = 16;
             smem_budget = dev.max_smem;
+            grid = B * 16;
         } else {
-            vi = 1;
-            smem_budget = dev.smem_per_sm / 2 - 1024;
+            for (int cs = 16; cs >= 2; cs /= 2) {
+                const int g = min(2 * sms / cs, dev.max_clusters[1][cs]);
+                if (g > 0 && (int64_t)g * cs >= B) {
+                    vi = 1;
+                    cluster = cs;
+                    smem_budget = dev.smem_per_sm / 2 - 1024;
+                    grid = g * cs;
+                    pl.grouped = 1;
+                    break;
+                }
+            }
         }
     }
     pl.v = &kVariants[vi];
@@ -987,7 +1166,7 @@ Plan make_plan(int32_t B, int32_t k, const DeviceInfo &dev)
     if (stage_cap < 2 * pl.win_cap) stage_cap = 2 * pl.win_cap;
     pl.stage_cap = stage_cap;
     pl.smem = pl.off_keys + stage_cap * 4;
-    pl.grid = B * cluster;
+    pl.grid = grid;
     return pl;
 }
 
@@ -1155,6 +1334,7 @@ int topk_ragged(const float *scores, int64_t n_scores, const int32_t *row_starts
     prm.win_cap = pl.win_cap;
     prm.off_win = pl.off_win;
     prm.off_keys = pl.off_keys;
+    prm.grouped = pl.grouped;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)pl.grid, 1, 1);

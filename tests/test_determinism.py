@@ -1,0 +1,106 @@
+"""Run-to-run and batch-composition determinism of the CUDA path.
+
+Repeats under scheduling noise (a busy sibling stream, the method of the tie
+study in sglang PR #31115) must be byte-identical, and a row's output must not
+depend on which rows share its batch: the batch size changes the launch shape
+(one CTA per row, grouped clusters, one cluster per row) and the grouped
+clusters deal CTAs to rows by length, so each row is split differently in
+each of these runs."""
+import hashlib
+
+import numpy as np
+import pytest
+import torch
+
+import sparse_attention_deterministic_gb300 as pkg
+import workloads as W
+from helpers import oracle_run
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    pkg.build()
+    pkg.init()
+
+
+def _run(scores, starts, lengths, k, mode, stream=None):
+    idx, val = pkg.topk_ragged(scores, starts, lengths, k, mode, with_values=True, stream=stream)
+    return idx, val
+
+
+def _digest(*ts):
+    h = hashlib.sha256()
+    for t in ts:
+        h.update(t.cpu().numpy().tobytes())
+    return h.hexdigest()
+
+
+@pytest.mark.parametrize("name", ["tiny", "decode", "adversarial"])
+def test_repeats_identical_under_noise(name):
+    w = W.make(name, device="cuda")
+    noise = torch.randn(2048, 2048, device="cuda")
+    side = torch.cuda.Stream()
+    main = torch.cuda.Stream()
+    digests = set()
+    for rep in range(100):
+        with torch.cuda.stream(side):
+            for _ in range(2):
+                noise = noise @ noise
+                noise = noise / noise.norm()
+        with torch.cuda.stream(main):
+            idx, val = _run(w.scores, w.row_starts, w.lengths, w.k, w.offset_mode, stream=main)
+        main.synchronize()
+        digests.add(_digest(idx, val))
+    torch.cuda.synchronize()
+    assert len(digests) == 1
+
+
+def _row_bytes(idx, val):
+    return [bytes(idx[i].cpu().numpy().tobytes()) + bytes(val[i].cpu().numpy().tobytes())
+            for i in range(idx.shape[0])]
+
+
+def test_batch_composition_invariance():
+    w = W.decode(B=64, k=2048).to("cuda")
+    base_idx, base_val = _run(w.scores, w.row_starts, w.lengths, w.k, 0)
+    base = _row_bytes(base_idx, base_val)
+    g = torch.Generator().manual_seed(3)
+    perm = torch.randperm(64, generator=g).cuda()
+    subsets = [perm, torch.arange(0, 64, 3).cuda(), torch.arange(1).cuda(), torch.tensor([63]).cuda(),
+               torch.arange(0, 8).cuda(), torch.arange(0, 20).cuda()]
+    for sel in subsets:
+        idx, val = _run(w.scores, w.row_starts[sel].contiguous(), w.lengths[sel].contiguous(), w.k, 0)
+        got = _row_bytes(idx, val)
+        for j, i in enumerate(sel.tolist()):
+            assert got[j] == base[i], (sel.numel(), i)
+    # Embed the rows in a batch large enough for the one-CTA-per-row shape.
+    rep = torch.arange(64, device="cuda").repeat(12)
+    idx, val = _run(w.scores, w.row_starts[rep].contiguous(), w.lengths[rep].contiguous(), w.k, 0)
+    got = _row_bytes(idx, val)
+    for j, i in enumerate(rep.tolist()):
+        assert got[j] == base[i]
+
+
+def test_launch_shapes_cover_all_variants():
+    shapes = {B: pkg.launch_info(B, 2048) for B in (1, 4, 64, 300, 400, 4096)}
+    assert shapes[4]["cluster"] == 16 and shapes[4]["threads"] == 1024
+    assert shapes[64]["threads"] == 512 and shapes[64]["cluster"] >= 2
+    assert shapes[4096]["cluster"] == 1 and shapes[4096]["grid"] == 4096
+    for info in shapes.values():
+        assert info["launches"] == 1
+
+
+@pytest.mark.parametrize("B", [300, 400])
+def test_batches_between_shapes(B):
+    g = torch.Generator().manual_seed(B)
+    lengths = torch.randint(0, 30000, (B,), generator=g).to(torch.int32)
+    starts = (torch.cumsum(lengths.to(torch.int64), 0) - lengths.to(torch.int64)).to(torch.int32)
+    scores = torch.relu(torch.randn(int(lengths.sum()), generator=g) - 0.3)
+    w = W.Workload(f"mid{B}", scores, starts, lengths, 2048, 1, {})
+    g_ = w.to("cuda")
+    idx, val = _run(g_.scores, g_.row_starts, g_.lengths, w.k, 1)
+    ref_idx, ref_val, _ = oracle_run(w)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    assert np.array_equal(val.cpu().numpy().view(np.uint32), ref_val)

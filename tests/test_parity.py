@@ -58,7 +58,7 @@ def test_random_bit_patterns(alphabet, B):
 
 # --- every k, every planner class, ragged lengths around k --------------------
 @pytest.mark.parametrize("k", [1, 2, 7, 100, 512, 1024, 2047, 2048, 3000, 4096])
-@pytest.mark.parametrize("B", [1, 5, 40, 160, 700])
+@pytest.mark.parametrize("B", [1, 5, 40, 160, 300, 400, 700])
 def test_lengths_around_k(k, B):
     g = torch.Generator().manual_seed(1000 * k + B)
     choices = [0, 1, 2, 3, 4, 5, k - 1, k, k + 1, 2 * k + 3, 4 * k + 1, 40000]
