@@ -34,7 +34,7 @@ extern "C" {
 
 #define TOPK_RAGGED_ABI_VERSION 1
 #define TOPK_RAGGED_MAX_K 4096
-/* Row lengths must stay below 2^24 (the pages' envelope "L < 2**24"). */
+/* Row lengths must stay below 2^24, the envelope of the 24-bit index field. */
 #define TOPK_RAGGED_MAX_LEN (1 << 24)
 
 /* Synchronous return codes. */

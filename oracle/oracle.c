@@ -13,17 +13,17 @@
  *   order       the bitwise total order on fp32 bit patterns: every pattern u
  *               maps to an unsigned 32-bit order key, larger key ranks first,
  *               and among bitwise-equal scores the smaller row-local index
- *               ranks first -- "score desc, index asc on bitwise-equal scores"
- *               with "NaN ordering (bitwise total order, not torch.topk
- *               NaN-maximal)" (sglang PR #31115 "Add opt-in deterministic
- *               CuTe-DSL DSA top-k backend", PR summary and the hardening
- *               commit message);
+ *               ranks first; NaNs take their place in that bit order
+ *               instead of all ranking first as in torch.topk (sglang PR
+ *               #31115 "Add opt-in deterministic CuTe-DSL DSA top-k
+ *               backend", PR summary and the hardening commit message);
  *   selection   the first n = min(k, L_i) entries of that order, which is the
  *               smallest-index subset of the tie set at the k-th boundary
  *               (same page, PR summary; Modifications);
  *   output      out_idx[i, p] = row-local index (offset_mode 0) or
  *               row_starts[i] + index (offset_mode 1) for p < n, -1 for
- *               p >= n ("front-packed, -1 padded", same page, Modifications;
+ *               p >= n (rows packed from the front and filled with -1, same
+ *               page, Modifications;
  *               the -1 padding when length < k also appears in the blog post
  *               "Non-deterministic Qwen3.8-Flash-Next: we found the faulty
  *               vLLM kernel and fixed it", section "The price of the fix");
@@ -31,11 +31,11 @@
  *               -inf bits (0xFF800000) in the padding (the pages name no pad
  *               value; -inf is this library's reading).
  *   envelope    a length >= 2^24 breaks the 24-bit inverted-index composite
- *               the pages' kernel relies on ("L >= 2**24 wraps nidx24", same
+ *               the pages' kernel relies on (the index field wraps; same
  *               page, hardening commit); such a row is written as all -1 and
  *               flagged (bit 1).  A window not inside [0, n_scores) is written
  *               as all -1 and flagged (bit 2): the flat-buffer reading of the
- *               "trusted-metadata window clamps" of the same commit.
+ *               same commit's clamping of windows against trusted metadata.
  *
  * Method: per row, build (order key, index) pairs and sort them with qsort
  * under an explicit comparator.  No blocking, no radix, no fusion.
@@ -54,7 +54,7 @@
  * clear) setting the sign bit moves it above every negative pattern while
  * keeping magnitude order; for a negative float, inverting all bits reverses
  * magnitude order (a larger magnitude is a smaller number) and clears the top
- * bit.  This is the "bitwise total order" the hardening commit names: -NaN
+ * bit.  This is the total order on bit patterns of the hardening commit: -NaN
  * below -inf, -0.0 just below +0.0, +NaN above +inf, NaN payloads ordered by
  * their bits. */
 uint32_t oracle_order_key(uint32_t bits)
