@@ -59,7 +59,6 @@ struct Params {
     int32_t win_cap;     // winner slots in the leader (power of two >= k - 1)
     int32_t off_win;     // byte offset of the winner array in dynamic smem
     int32_t off_keys;    // byte offset of the staged keys in dynamic smem
-    int32_t grouped;     // clusters take groups of rows (see assign_rows)
 };
 
 // Per-CTA control block at the start of dynamic shared memory.
@@ -68,18 +67,21 @@ struct __align__(16) Ctrl {
     uint32_t sel_gt;     //   entries above the chosen bin (within the prefix)
     uint32_t sel_cnt;    //   entries in the chosen bin
     uint32_t sel_done;   //   1: the k-th key is +0.0 (plateau shortcut)
-    uint32_t zeros;      // this CTA's count of exact +0.0 scores
-    uint32_t zeros_tot;  // leader: the cluster's count of exact +0.0 scores
-    uint32_t win_count;  // leader: winner slots handed out
-    uint32_t pad;
-    uint32_t kmax;       // this CTA's largest order key
-    uint32_t kmax_tot;   // leader: the cluster's largest order key
-    uint32_t wmin;       // leader: the smallest winner key
-    uint32_t pad2;
+    uint32_t zeros;      // count of exact +0.0 scores
+    uint32_t win_count;  // winner slots handed out
+    uint32_t kmax;       // the largest order key
+    uint32_t wmin;       // the smallest winner key
     uint32_t warp_zeros[32];
     uint32_t warp_ties[32];
     uint32_t scan[36];
     uint64_t scan64[32];
+    // Short-row path: per-warp partials (entries above +0.0, +0.0 count,
+    // smallest and largest non-zero key) and the bucket statistics.
+    uint32_t part_p[32], part_z[32], part_min[32], part_max[32];
+    uint32_t sq;         // sum of squared sizes of the buckets that are output
+    uint32_t npart;      // entries in those buckets
+    uint32_t tot_p;      // entries above +0.0
+    uint32_t tot_z;      // +0.0 entries
 };
 
 // ------------------------------------------------------------------------- //
@@ -138,11 +140,6 @@ __device__ __forceinline__ uint32_t dsmem_addr(const void *p, uint32_t rank)
     return remote;
 }
 
-__device__ __forceinline__ void dsmem_red_add(uint32_t addr, uint32_t v)
-{
-    asm volatile("red.shared::cluster.add.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
 __device__ __forceinline__ uint32_t dsmem_atom_add(uint32_t addr, uint32_t v)
 {
     uint32_t old;
@@ -172,9 +169,74 @@ __device__ __forceinline__ uint32_t dsmem_ld(uint32_t addr)
     return v;
 }
 
-__device__ __forceinline__ void dsmem_st(uint32_t addr, uint32_t v)
+__device__ __forceinline__ void dsmem_ld_bins(uint32_t addr, uint32_t (&v)[2])
 {
-    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+    asm volatile("ld.shared::cluster.v2.u32 {%0, %1}, [%2];" : "=r"(v[0]), "=r"(v[1]) : "r"(addr) : "memory");
+}
+
+__device__ __forceinline__ void dsmem_ld_bins(uint32_t addr, uint32_t (&v)[4])
+{
+    asm volatile("ld.shared::cluster.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]) : "r"(addr) : "memory");
+}
+
+// ------------------------------------------------------------------------- //
+// mbarrier and bulk-copy (TMA) primitives (inline PTX).
+// ------------------------------------------------------------------------- //
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return (uint32_t)__cvta_generic_to_shared(p);
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+    // Make the initialised barrier visible to the bulk-copy (async) proxy.
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, uint32_t bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity)
+{
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+
+// Global -> shared bulk copy that completes `bytes` of transactions on
+// `bar`.  dst and src 16-byte aligned, bytes a multiple of 16.
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar)
+{
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+                 ::"r"(smem_addr(dst)), "l"(src), "r"(bytes), "r"(smem_addr(bar))
+                 : "memory");
+}
+
+// Bounded wait for phase `parity` of `bar`.  A copy that never lands is a
+// hardware or library fault: the status word records it, and a second
+// bounded wait gives the copies in flight time to finish before the CTA
+// goes on, so that no late copy can land in reused shared memory.
+constexpr uint32_t kWaitLimit = 1u << 22;
+
+__device__ __forceinline__ void mbar_wait_bounded(uint64_t *bar, uint32_t parity)
+{
+    for (uint32_t i = 0; i < kWaitLimit; ++i)
+        if (mbar_try_wait(bar, parity)) return;
+    atomicOr(&g_status, TOPK_DEV_INTERNAL);
+    for (uint32_t i = 0; i < kWaitLimit; ++i)
+        if (mbar_try_wait(bar, parity)) return;
 }
 
 // ------------------------------------------------------------------------- //
@@ -396,10 +458,11 @@ __device__ __forceinline__ uint64_t block_incl_scan64(uint64_t x, uint64_t *sm, 
 // bucket start plus the number of bucket members above it, so the result
 // depends only on the composites.  Work is n + sum(m_b^2); when the buckets
 // are too skewed for that to stay small the function sorts with a bitonic
-// network instead.  b[] is scratch for n composites, cur[] kBins words.
+// network instead.  Only the first n_out places are written.  b[] is
+// scratch for n composites, cur[] kBins words.
 // ------------------------------------------------------------------------- //
 template <int THREADS>
-__device__ void sort_and_write(uint64_t *a, uint64_t *b, int n, int cap_pow2, uint32_t kmin,
+__device__ void sort_and_write(uint64_t *a, uint64_t *b, int n, int n_out, int cap_pow2, uint32_t kmin,
                                uint32_t kmax, uint32_t *cur, uint64_t *sm64, int32_t *oi, float *ov,
                                int64_t idx_offset)
 {
@@ -428,7 +491,7 @@ __device__ void sort_and_write(uint64_t *a, uint64_t *b, int n, int cap_pow2, ui
         for (int i = n + tid; i < n2; i += THREADS) a[i] = 0ull;
         __syncthreads();
         bitonic_desc<THREADS>(a, (uint32_t)n2);
-        for (int p = tid; p < n; p += THREADS) {
+        for (int p = tid; p < n_out; p += THREADS) {
             const uint64_t c = a[p];
             oi[p] = (int32_t)(idx_offset + (int32_t)(~(uint32_t)c));
             if (ov) ov[p] = __uint_as_float(key_bits((uint32_t)(c >> 32)));
@@ -457,8 +520,10 @@ __device__ void sort_and_write(uint64_t *a, uint64_t *b, int n, int cap_pow2, ui
         uint32_t rank = 0;
         for (uint32_t q = st; q < en; ++q) rank += b[q] > x;
         const uint32_t pos = st + rank;
-        oi[pos] = (int32_t)(idx_offset + (int32_t)(~(uint32_t)x));
-        if (ov) ov[pos] = __uint_as_float(key_bits((uint32_t)(x >> 32)));
+        if (pos < (uint32_t)n_out) {
+            oi[pos] = (int32_t)(idx_offset + (int32_t)(~(uint32_t)x));
+            if (ov) ov[pos] = __uint_as_float(key_bits((uint32_t)(x >> 32)));
+        }
     }
 }
 
@@ -468,6 +533,231 @@ __device__ __forceinline__ void pad_out(int32_t *oi, float *ov, int from, int to
         oi[p] = -1;
         if (ov) ov[p] = __uint_as_float(kNegInfBits);
     }
+}
+
+// ------------------------------------------------------------------------- //
+// Short rows: one CTA per row with the whole row in registers (at most
+// kShortQuads quads per thread).  Canonical order cuts a row at the order
+// key of +0.0 into P (keys above it), the +0.0 entries and N (keys below
+// it), and lists P in key order, then the +0.0 entries by index, then N in
+// key order.  The non-zero entries are ranked together by one bucket pass
+// over their own key range: 2 x kBins buckets of 2^sh keys (16-bit counters, two
+// to a word), bucket starts from a
+// scan, every entry dropped into its bucket, and its place the bucket start
+// plus the number of members of its bucket above it (composites are unique,
+// so this is exact).  Buckets that start at or after k are never output and
+// are not ranked.  An N entry moves down by the +0.0 count; a +0.0 entry's
+// place is |P| plus its ordinal in index order, from per-warp ballots.  So a
+// row costs one read, two shared-memory atomics per non-zero entry and no
+// radix levels.  When the output buckets are too big for member counting to
+// stay cheap (heavy ties off +0.0) or overflow the scratch, the function
+// returns false with shared memory released and the general path runs.
+// ------------------------------------------------------------------------- //
+constexpr int kShortQuads = 4;
+constexpr int kShortBucketBits = 12;   // 2 * kBins buckets with 16-bit counters
+
+template <int THREADS>
+__device__ bool short_row(Ctrl &ctrl, uint32_t *cur, uint64_t *buf, uint32_t buf_cap, const Slice &s,
+                          uint32_t k_eff, int64_t idx_offset, int32_t *oi, float *ov, int k)
+{
+    constexpr int NW = THREADS / 32;
+    constexpr int BPT = kBins / THREADS;
+    constexpr uint32_t kZ = 0x80000000u;   // order key of +0.0
+    static_assert(kShortQuads * NW <= 32, "one (quad round, warp) count per lane of warp 0");
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint32_t lt = lanemask_lt();
+
+    // Thread t holds quads t, t + THREADS, ...: index order is round u, then
+    // warp, then lane, then slot.  Round u of a warp holds data iff
+    // active(u); the test is warp-uniform.
+    auto active = [&](int u) { return warp * 32 + u * THREADS < s.nq; };
+    uint32_t key[kShortQuads][4];
+    uint32_t vm[kShortQuads];
+#pragma unroll
+    for (int u = 0; u < kShortQuads; ++u) {
+        const int q = tid + u * THREADS;
+        vm[u] = 0;
+        uint4 kk = make_uint4(0, 0, 0, 0);
+        if (q < s.nq) kk = load_quad_global(s, q, vm[u]);
+        key[u][0] = kk.x; key[u][1] = kk.y; key[u][2] = kk.z; key[u][3] = kk.w;
+    }
+    for (int b = tid; b < kBins; b += THREADS) cur[b] = 0u;
+    if (tid == 0) {
+        ctrl.sq = 0u;
+        ctrl.npart = 0u;
+    }
+    // Per round: the +0.0 slots (zm, 4 bits a round) and the non-zero slots
+    // (nm); their per-warp +0.0 counts in index order go to warp_zeros.
+    uint32_t zm = 0, nm = 0, pc = 0, kmin = kFull, kmax = 0;
+#pragma unroll
+    for (int u = 0; u < kShortQuads; ++u) {
+        if (!active(u)) continue;
+        uint32_t z = 0, n = 0;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t e = key[u][i];
+            const bool v = (vm[u] >> i) & 1u;
+            z |= (uint32_t)(v && e == kZ) << i;
+            n |= (uint32_t)(v && e != kZ) << i;
+            pc += v && e > kZ;
+            if (v && e != kZ) {
+                kmin = min(kmin, e);
+                kmax = max(kmax, e);
+            }
+        }
+        zm |= z << (4 * u);
+        nm |= n << (4 * u);
+        const uint32_t zw = __reduce_add_sync(kFull, (uint32_t)__popc(z));
+        if (lane == 0) ctrl.warp_zeros[u * NW + warp] = zw;
+    }
+    pc = __reduce_add_sync(kFull, pc);
+    kmin = __reduce_min_sync(kFull, kmin);
+    kmax = __reduce_max_sync(kFull, kmax);
+    if (lane == 0) {
+        ctrl.part_p[warp] = pc;
+        ctrl.part_min[warp] = kmin;
+        ctrl.part_max[warp] = kmax;
+    }
+    if (lane < kShortQuads && !active(lane)) ctrl.warp_zeros[lane * NW + warp] = 0u;
+    __syncthreads();
+
+    uint32_t nzmin = kFull, nzmax = 0;
+#pragma unroll
+    for (int w = 0; w < NW; w += 4) {
+        const uint4 a = *reinterpret_cast<const uint4 *>(&ctrl.part_min[w]);
+        const uint4 b = *reinterpret_cast<const uint4 *>(&ctrl.part_max[w]);
+        nzmin = min(min(nzmin, min(a.x, a.y)), min(a.z, a.w));
+        nzmax = max(max(nzmax, max(b.x, b.y)), max(b.z, b.w));
+    }
+    const bool any_nz = nzmin <= nzmax;   // CTA-uniform
+    const int sh = any_nz ? max(0, (32 - __clz(nzmax - nzmin)) - kShortBucketBits) : 0;
+#pragma unroll
+    for (int u = 0; u < kShortQuads; ++u) {
+        if (!active(u) || !__any_sync(kFull, (nm >> (4 * u)) & 0xFu)) continue;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if ((nm >> (4 * u + i)) & 1u) {
+                const uint32_t d = (key[u][i] - nzmin) >> sh;
+                atomicAdd(&cur[d >> 1], 1u << ((d & 1u) << 4));
+            }
+        }
+    }
+    if (warp == 0) {
+        // Exclusive bases of the (round, warp) +0.0 counts in index order,
+        // and the row totals.
+        const uint32_t z = lane < kShortQuads * NW ? ctrl.warp_zeros[lane] : 0u;
+        const uint32_t zi = warp_incl_scan(z);
+        if (lane < kShortQuads * NW) ctrl.warp_ties[lane] = zi - z;
+        const uint32_t pp = __reduce_add_sync(kFull, lane < NW ? ctrl.part_p[lane] : 0u);
+        if (lane == 31) {
+            ctrl.tot_z = zi;
+            ctrl.tot_p = pp;
+        }
+    }
+    __syncthreads();
+
+    const uint32_t P = ctrl.tot_p, Zc = ctrl.tot_z;
+    // The +0.0 entries go to P + their ordinal in index order.
+    if (Zc > 0 && P < k_eff) {
+#pragma unroll
+        for (int u = 0; u < kShortQuads; ++u) {
+            const uint32_t z = (zm >> (4 * u)) & 0xFu;
+            if (!active(u) || !__any_sync(kFull, z)) continue;
+            const int32_t j0 = (int32_t)idx_offset + s.jbase + 4 * (tid + u * THREADS);
+            uint32_t ord = P + ctrl.warp_ties[u * NW + warp];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ord += (uint32_t)__popc(__ballot_sync(kFull, (z >> i) & 1u) & lt);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint32_t o = ord + (uint32_t)__popc(z & ((1u << i) - 1u));
+                if (((z >> i) & 1u) && o < k_eff) oi[o] = j0 + i;
+            }
+            if (ov) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const uint32_t o = ord + (uint32_t)__popc(z & ((1u << i) - 1u));
+                    if (((z >> i) & 1u) && o < k_eff) ov[o] = 0.0f;
+                }
+            }
+        }
+    }
+    if (any_nz) {
+        // Bucket starts, top bucket first (in a word the high half is the
+        // higher bucket); the buckets that start below k are the ones output.
+        const int lo = kBins - (tid + 1) * BPT;
+        uint32_t v[BPT];
+        load_bins<THREADS>(cur, lo, v);
+        uint32_t sum = 0;
+#pragma unroll
+        for (int i = 0; i < BPT; ++i) sum += (v[i] >> 16) + (v[i] & 0xFFFFu);
+        uint32_t run = block_incl_scan<THREADS>(sum, ctrl.scan) - sum;
+        uint32_t sq = 0, np = 0;
+#pragma unroll
+        for (int i = BPT - 1; i >= 0; --i) {
+            const uint32_t hi = v[i] >> 16, lo16 = v[i] & 0xFFFFu;
+            const uint32_t st_hi = run, st_lo = run + hi;
+            if (st_hi < k_eff) {
+                sq += hi * hi;
+                np += hi;
+            }
+            if (st_lo < k_eff) {
+                sq += lo16 * lo16;
+                np += lo16;
+            }
+            cur[lo + i] = (st_hi << 16) | st_lo;
+            run = st_lo + lo16;
+        }
+        sq = __reduce_add_sync(kFull, sq);
+        np = __reduce_add_sync(kFull, np);
+        if (lane == 0 && np) {
+            atomicAdd(&ctrl.sq, sq);
+            atomicAdd(&ctrl.npart, np);
+        }
+    }
+    __syncthreads();
+    const uint32_t npart = ctrl.npart;
+    if (npart > buf_cap || ctrl.sq > 32u * npart + 4096u) {   // CTA-uniform
+        __syncthreads();
+        return false;
+    }
+    if (npart) {
+#pragma unroll
+        for (int u = 0; u < kShortQuads; ++u) {
+            if (!active(u) || !__any_sync(kFull, (nm >> (4 * u)) & 0xFu)) continue;
+            const uint32_t nj0 = ~(uint32_t)(s.jbase + 4 * (tid + u * THREADS));
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if ((nm >> (4 * u + i)) & 1u) {
+                    const uint32_t e = key[u][i];
+                    const uint32_t d = (e - nzmin) >> sh, hs = (d & 1u) << 4;
+                    const uint32_t pos = (atomicAdd(&cur[d >> 1], 1u << hs) >> hs) & 0xFFFFu;
+                    if (pos < npart) buf[pos] = ((uint64_t)e << 32) | (uint64_t)(nj0 - (uint32_t)i);
+                }
+            }
+        }
+        __syncthreads();
+        // Bucket d's counter now holds its end, and the start of bucket d
+        // is the end of bucket d + 1.
+#pragma unroll 1
+        for (uint32_t x = tid; x < npart; x += THREADS) {
+            const uint64_t c = buf[x];
+            const uint32_t e = (uint32_t)(c >> 32);
+            const uint32_t d = (e - nzmin) >> sh;
+            const uint32_t w = cur[d >> 1];
+            const uint32_t en = (d & 1u) ? (w >> 16) : (w & 0xFFFFu);
+            const uint32_t st = (d & 1u) ? (d + 1 < 2u * kBins ? cur[(d + 1) >> 1] & 0xFFFFu : 0u) : (w >> 16);
+            uint32_t pos = st;
+#pragma unroll 1
+            for (uint32_t y = st; y < en; ++y) pos += buf[y] > c;
+            if (e < kZ) pos += Zc;
+            if (pos < k_eff) {
+                oi[pos] = (int32_t)(idx_offset + (int32_t)(~(uint32_t)c));
+                if (ov) ov[pos] = __uint_as_float(key_bits(e));
+            }
+        }
+    }
+    pad_out(oi, ov, (int)k_eff, k);
+    return true;
 }
 
 // Quads of warp `warp`'s contiguous segment of the slice.
@@ -494,6 +784,8 @@ struct RowGroup {
     int row;        // my row, or -1 when the cluster has no row with work
     uint32_t g0;    // cluster rank of the group's first CTA (its leader)
     uint32_t gsize; // CTAs working on the row
+    int32_t start;  // the row's row_starts and valid length
+    int32_t len;
 };
 
 __device__ __forceinline__ bool row_window_ok(const Params &p, int i, int64_t &len)
@@ -507,59 +799,61 @@ __device__ __forceinline__ bool row_window_ok(const Params &p, int i, int64_t &l
 
 template <int THREADS>
 __device__ RowGroup assign_rows(const Params &p, uint32_t crank, uint32_t csize, uint32_t *scratch,
-                                uint32_t *slot)
+                                uint32_t *work, uint32_t *slot)
 {
     const int tid = threadIdx.x;
-    const int B = p.B;
+    const int B = p.B;   // at most 512 (the planner's cluster shapes hold fewer CTAs)
     const int G = (int)(gridDim.x / csize), cid = (int)(blockIdx.x / csize);
     uint32_t *eff = scratch;              // B valid lengths (0: nothing to select)
+    uint32_t *starts = scratch + 512;     // B row starts
     uint32_t *by_rank = scratch + 1024;   // row index of every rank
     for (int i = tid; i < B; i += THREADS) {
         int64_t len;
         eff[i] = row_window_ok(p, i, len) ? (uint32_t)len : 0u;
+        starts[i] = (uint32_t)p.row_starts[i];
     }
+    for (int i = B + tid; i < ((B + 3) & ~3); i += THREADS) eff[i] = 0u;   // pad to whole vectors
     __syncthreads();
     for (int i = tid; i < B; i += THREADS) {
         const uint32_t e = eff[i];
         int rank = 0;
-        for (int j = 0; j < B; ++j) {
-            const uint32_t ej = eff[j];
-            rank += (ej > e) || (ej == e && j < i);
+        for (int j = 0; j < B; j += 4) {
+            const uint4 q = *reinterpret_cast<const uint4 *>(eff + j);
+            rank += (q.x > e || (q.x == e && j < i)) + (q.y > e || (q.y == e && j + 1 < i)) +
+                    (q.z > e || (q.z == e && j + 2 < i)) + (q.w > e || (q.w == e && j + 3 < i));
         }
         by_rank[rank] = (uint32_t)i;
     }
     __syncthreads();
     if (tid == 0) {
-        int rows[16];
-        uint32_t len[16];
+        // The cluster's rows, their lengths and CTA counts (at most 16 each).
+        uint32_t *rows = work, *len = work + 16, *c = work + 32;
         int m = 0;
         for (int t0 = 0; t0 < B; t0 += 2 * G) {
             const int ta = t0 + cid, tb = t0 + 2 * G - 1 - cid;
-            if (ta < B && m < 16) { rows[m] = (int)by_rank[ta]; len[m] = eff[rows[m]]; ++m; }
-            if (tb < B && m < 16) { rows[m] = (int)by_rank[tb]; len[m] = eff[rows[m]]; ++m; }
+            if (ta < B && m < 16) { rows[m] = by_rank[ta]; len[m] = eff[rows[m]]; ++m; }
+            if (tb < B && m < 16) { rows[m] = by_rank[tb]; len[m] = eff[rows[m]]; ++m; }
         }
-        // Rows are listed in rank order, so the rows with work come first.
+        // Rows are listed in rank order, so the rows with work come first;
+        // a cluster holds at most csize of them (the planner guarantees it).
         int mv = 0;
-        uint64_t E = 0;
-        while (mv < m && len[mv] > 0) E += len[mv++];
+        while (mv < m && mv < (int)csize && len[mv] > 0) ++mv;
         int mine = -1;
         uint32_t g0 = 0, gsize = 0;
         if (mv > 0) {
-            uint32_t c[16];
-            uint32_t used = 0;
-            const uint32_t spare = csize - (uint32_t)mv;
-            for (int i = 0; i < mv; ++i) {
-                c[i] = 1u + (uint32_t)((uint64_t)spare * len[i] / E);
-                used += c[i];
-            }
-            for (int i = 0; used < csize; i = (i + 1) % mv) {
-                ++c[i];
-                ++used;
+            // One CTA per row, then each spare CTA to the row with the
+            // largest slice (len / c; ties to the earlier row).
+            for (int i = 0; i < mv; ++i) c[i] = 1u;
+            for (uint32_t used = (uint32_t)mv; used < csize; ++used) {
+                int best = 0;
+                for (int i = 1; i < mv; ++i)
+                    if ((uint64_t)len[i] * c[best] > (uint64_t)len[best] * c[i]) best = i;
+                ++c[best];
             }
             uint32_t start = 0;
             for (int i = 0; i < mv; ++i) {
                 if (crank >= start && crank < start + c[i]) {
-                    mine = rows[i];
+                    mine = (int)rows[i];
                     g0 = start;
                     gsize = c[i];
                 }
@@ -571,13 +865,15 @@ __device__ RowGroup assign_rows(const Params &p, uint32_t crank, uint32_t csize,
         slot[2] = gsize;
         // The cluster's first CTA pads the rows with nothing to select.
         slot[3] = (uint32_t)(m - mv);
-        for (int i = mv; i < m; ++i) slot[4 + i - mv] = (uint32_t)rows[i];
+        for (int i = mv; i < m; ++i) slot[4 + i - mv] = rows[i];
     }
     __syncthreads();
     RowGroup g;
     g.row = (int)slot[0];
     g.g0 = slot[1];
     g.gsize = slot[2];
+    g.start = g.row >= 0 ? (int32_t)starts[g.row] : 0;
+    g.len = g.row >= 0 ? (int32_t)eff[g.row] : 0;
     if (crank == 0) {
         const int npad = (int)slot[3];
         for (int i = 0; i < npad; ++i) {
@@ -596,18 +892,20 @@ __device__ RowGroup assign_rows(const Params &p, uint32_t crank, uint32_t csize,
 }
 
 // ------------------------------------------------------------------------- //
-// The kernel.  CLUSTER = false: one row per CTA.  CLUSTER = true: each
-// cluster takes a group of rows (assign_rows) and every row is worked on by
-// a contiguous group of the cluster's CTAs; the group's first CTA is the
-// row's leader (cluster-wide histograms, threshold search, winner list,
-// sort).  With one row per cluster the group is the whole cluster.
+// The one-CTA-per-row kernel, for batches of many rows.  A row that fits the
+// registers takes short_row; any other row (or a short row whose buckets are
+// too skewed) takes the general path below: the row is streamed once into
+// shared memory (what does not fit is re-read from L2), an MSB-first radix
+// select of 11, 11 and 10 bits finds the exact k-th key T, the winners
+// (key > T) are gathered and sorted, and the first r ties (key == T) are
+// placed by index.
 //
-// Every pass over a CTA's slice walks the same contiguous per-warp
-// segments, U quads per lane in flight, so per-warp counts taken in one pass
-// give index-ordered positions in a later one.
+// Every pass over the slice walks the same contiguous per-warp segments, U
+// quads per lane in flight, so per-warp counts taken in one pass give
+// index-ordered positions in a later one.
 // ------------------------------------------------------------------------- //
-template <int THREADS, bool CLUSTER>
-__global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kernel(const Params p)
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_row_kernel(const Params p)
 {
     constexpr int NW = THREADS / 32;
     constexpr int U = 4;                       // quads in flight per lane
@@ -616,31 +914,11 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
     extern __shared__ __align__(16) unsigned char smem[];
     Ctrl &ctrl = *reinterpret_cast<Ctrl *>(smem);
     uint32_t *hist = reinterpret_cast<uint32_t *>(smem + sizeof(Ctrl));
-    uint32_t *hist_tot = hist + kBins;   // the row leader's group-wide histogram (CLUSTER only)
     uint64_t *win = reinterpret_cast<uint64_t *>(smem + p.off_win);
     uint32_t *keys = reinterpret_cast<uint32_t *>(smem + p.off_keys);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    int row;
-    uint32_t grank = 0, gsize = 1, g0 = 0;
-    if (CLUSTER) {
-        const uint32_t crank = cluster_rank(), csize = cluster_size();
-        if (p.grouped) {
-            const RowGroup g = assign_rows<THREADS>(p, crank, csize, hist, ctrl.scan);
-            if (g.row < 0) return;   // uniform over the cluster: nothing to select
-            row = g.row;
-            g0 = g.g0;
-            gsize = g.gsize;
-            grank = crank - g0;
-        } else {
-            row = (int)(blockIdx.x / csize);
-            gsize = csize;
-            grank = crank;
-        }
-    } else {
-        row = (int)blockIdx.x;
-    }
-    const bool leader = grank == 0;
+    const int row = (int)blockIdx.x;
 
     // ---- a1: metadata, window checks ----------------------------------- //
     const int64_t rs = p.row_starts[row];
@@ -654,13 +932,8 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
     int32_t *oi = p.out_idx + (int64_t)row * p.k;
     float *ov = p.out_val ? p.out_val + (int64_t)row * p.k : nullptr;
     if (bad || len == 0) {
-        // Grouped clusters never get here (such rows are padded above); with
-        // one row per cluster the decision is uniform over the cluster and
-        // precedes every cluster barrier.
-        if (leader) {
-            if (bad && tid == 0) atomicOr(&g_status, bad);
-            pad_out(oi, ov, 0, p.k);
-        }
+        if (bad && tid == 0) atomicOr(&g_status, bad);
+        pad_out(oi, ov, 0, p.k);
         return;
     }
     const int32_t L = (int32_t)len;
@@ -675,10 +948,8 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
         int64_t a0 = e0 + (int64_t)((4u - (uint32_t)((pa + (uint64_t)e0) & 3u)) & 3u);
         if (a0 > e1) a0 = e1;
         const int64_t n4 = (e1 - a0) >> 2;
-        const int64_t qlo = n4 * grank / gsize, qhi = n4 * (grank + 1) / gsize;
-        const int64_t hb = a0 + 4 * qlo, he = a0 + 4 * qhi;
-        const int64_t glo = grank == 0 ? e0 : hb;
-        const int64_t ghi = grank == gsize - 1 ? e1 : he;
+        const int64_t hb = a0, he = a0 + 4 * n4;
+        const int64_t glo = e0, ghi = e1;
         const int64_t sbase = hb - ((hb - glo + 3) & ~(int64_t)3);
         s.gptr = p.scores + sbase;
         s.off0 = (int32_t)(glo - sbase);
@@ -689,27 +960,25 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
         s.sq = s.nq < (p.stage_cap >> 2) ? s.nq : (p.stage_cap >> 2);
         s.jbase = (int32_t)(sbase - rs);
     }
+    if (s.nq <= kShortQuads * THREADS) {
+        const uint32_t cap = (uint32_t)(p.off_keys + p.stage_cap * 4 - p.off_win) / 8u;
+        if (short_row<THREADS>(ctrl, hist, win, cap, s, k_eff, idx_offset, oi, ov, p.k)) return;
+    }
     const WarpSeg seg = warp_segment<THREADS>(s.nq, warp);
 
     // ---- init shared state ------------------------------------------------ //
-    for (int b = tid; b < kBins; b += THREADS) {
-        hist[b] = 0u;
-        if (CLUSTER && leader) hist_tot[b] = 0u;
-    }
+    for (int b = tid; b < kBins; b += THREADS) hist[b] = 0u;
     if (tid == 0) {
         ctrl.sel_digit = 0u;
         ctrl.sel_gt = 0u;
         ctrl.sel_cnt = 0u;
         ctrl.sel_done = 0u;
         ctrl.zeros = 0u;
-        ctrl.zeros_tot = 0u;
         ctrl.win_count = 0u;
         ctrl.kmax = 0u;
-        ctrl.kmax_tot = 0u;
         ctrl.wmin = kFull;
     }
     __syncthreads();
-    if (CLUSTER) cluster_arrive();   // B0: every CTA started and zeroed (waited before the flush)
 
     // ---- a2+a3: stream the slice once: key transform, stage, top-digit
     //      histogram, the largest key and per-warp counts of exact +0.0 --- //
@@ -750,16 +1019,12 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
     }
     __syncthreads();
 
-    const uint32_t lead_hist_tot = CLUSTER ? dsmem_addr(hist_tot, g0) : 0u;
-
-    // Running selection state (identical in every thread of the group).
+    // Running selection state (identical in every thread).
     uint32_t prefix = 0, n_gt = 0, r = k_eff, cnt = 0;
     bool plateau = false;   // T is +0.0, found from the zero count
     bool sel_done = false;  // the k-th key is known
 
-    // ---- a4+a5: radix levels of 11, 11 and 10 bits.  In a cluster every
-    //      CTA runs all three levels' barriers, working or not, because the
-    //      cluster's rows may finish at different levels. --------------- //
+    // ---- a4+a5: radix levels of 11, 11 and 10 bits --------------------- //
 #pragma unroll 1
     for (int level = 0; level < 3; ++level) {
         const int dbits = level == 2 ? 10 : 11;
@@ -791,52 +1056,17 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
             __syncthreads();
         }
         uint32_t d = 0, gt = 0, c = 0;
-        const uint32_t *htot = hist;
-        if (CLUSTER) {
-            if (level == 0) cluster_wait();   // B0 complete: the leaders' totals are zeroed
-            if (!sel_done) {
-                for (int b = tid; b < kBins; b += THREADS) {
-                    const uint32_t v = hist[b];
-                    if (v) dsmem_red_add(lead_hist_tot + 4u * (uint32_t)b, v);
-                }
-                if (level == 0 && tid == 0) {
-                    if (ctrl.zeros) dsmem_red_add(dsmem_addr(&ctrl.zeros_tot, g0), ctrl.zeros);
-                    dsmem_red_max(dsmem_addr(&ctrl.kmax_tot, g0), ctrl.kmax);
-                }
-            }
-            cluster_sync();   // B1: each leader holds its group's histogram
-            htot = hist_tot;
-        }
-        if ((!CLUSTER || leader) && !sel_done) {
-            if (find_bin<THREADS>(htot, r, ctrl.scan, d, gt, c)) {
+        if (!sel_done) {
+            if (find_bin<THREADS>(hist, r, ctrl.scan, d, gt, c)) {
                 // Plateau shortcut: the boundary bin holds only exact +0.0, so
                 // the k-th key is +0.0 and the finer levels are not needed.
-                const uint32_t ztot = CLUSTER ? ctrl.zeros_tot : ctrl.zeros;
-                const uint32_t done = (level == 0 && d == kZeroDigit && c == ztot) ? 1u : 0u;
-                if (CLUSTER) {
-                    for (uint32_t rk = g0; rk < g0 + gsize; ++rk) {
-                        dsmem_st(dsmem_addr(&ctrl.sel_digit, rk), d);
-                        dsmem_st(dsmem_addr(&ctrl.sel_gt, rk), gt);
-                        dsmem_st(dsmem_addr(&ctrl.sel_cnt, rk), c);
-                        dsmem_st(dsmem_addr(&ctrl.sel_done, rk), done);
-                    }
-                } else {
-                    ctrl.sel_digit = d;
-                    ctrl.sel_gt = gt;
-                    ctrl.sel_cnt = c;
-                    ctrl.sel_done = done;
-                }
+                ctrl.sel_digit = d;
+                ctrl.sel_gt = gt;
+                ctrl.sel_cnt = c;
+                ctrl.sel_done = (level == 0 && d == kZeroDigit && c == ctrl.zeros) ? 1u : 0u;
             }
         }
-        if (CLUSTER) {
-            if (leader && !sel_done) {
-                __syncthreads();
-                for (int b = tid; b < kBins; b += THREADS) hist_tot[b] = 0u;
-            }
-            cluster_sync();   // B2: selections visible to every CTA of their group
-        } else {
-            __syncthreads();
-        }
+        __syncthreads();
         if (!sel_done) {
             d = ctrl.sel_digit;
             gt = ctrl.sel_gt;
@@ -864,31 +1094,19 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
             }
         }
         __syncthreads();
-        if (!CLUSTER && sel_done) break;
+        if (sel_done) break;
     }
     const uint32_t T = prefix;   // exact k-th key; n_gt above it, take r of its cnt ties
     const uint32_t tval = key_bits(T);
 
     // ---- a6+a7: one pass over the slice.  Winners (key > T) go to the
-    //      leader's list in any order (their composites are unique, the sort
-    //      makes the order canonical).  Ties (key == T): the first r in
-    //      group-wide index order go straight to positions n_gt + ordinal.
-    //      On the plateau every tie is a +0.0 and the per-warp zero counts of
-    //      the streaming pass already give each warp's first ordinal; else
-    //      the pass counts ties per warp and a second pass writes them. --- //
-    uint32_t tie_base = 0, local_eq = cnt;
-    if (CLUSTER) {
-        local_eq = plateau ? ctrl.zeros : hist[T & 0x3FFu];
-        uint32_t part = 0;
-        if (warp == 0 && lane < (int)grank) {
-            const void *src = plateau ? (const void *)&ctrl.zeros : (const void *)&hist[T & 0x3FFu];
-            part = dsmem_ld(dsmem_addr(src, g0 + (uint32_t)lane));
-        }
-        if (warp == 0) part = __reduce_add_sync(kFull, part);
-        if (tid == 0) ctrl.scan[0] = part;
-        __syncthreads();
-        tie_base = ctrl.scan[0];
-    }
+    //      list in any order (their composites are unique, the sort makes
+    //      the order canonical).  Ties (key == T): the first r in index
+    //      order go straight to positions n_gt + ordinal.  On the plateau
+    //      every tie is a +0.0 and the per-warp zero counts of the streaming
+    //      pass already give each warp's first ordinal; else the pass counts
+    //      ties per warp and a second pass writes them. ------------------- //
+    const uint32_t tie_base = 0, local_eq = cnt;
     const bool want_ties = local_eq > 0 && tie_base < r;   // CTA-uniform
     uint32_t trun = 0;   // this warp's next tie ordinal (plateau)
     if (plateau && want_ties) {
@@ -901,8 +1119,6 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
         trun = tie_base + ctrl.warp_ties[warp];
     }
     const bool fused_ties = plateau && want_ties && ctrl.warp_zeros[warp] > 0;   // warp-uniform
-    const uint32_t win_count_addr = CLUSTER ? dsmem_addr(&ctrl.win_count, g0) : 0u;
-    const uint32_t win_addr = CLUSTER ? dsmem_addr(win, g0) : 0u;
     uint32_t ties_w = 0, wmin = kFull;
     int first_tie_q = seg.q1;
     const uint32_t lt = lanemask_lt();
@@ -941,7 +1157,7 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
                 }
                 uint32_t base = 0;
                 if (lane == 0)
-                    base = CLUSTER ? dsmem_atom_add(win_count_addr, wtot) : atomicAdd(&ctrl.win_count, wtot);
+                    base = atomicAdd(&ctrl.win_count, wtot);
                 slot += __shfl_sync(kFull, base, 0);
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
@@ -949,10 +1165,7 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
                         const uint32_t j = (uint32_t)(s.jbase + 4 * q + i);
                         const uint64_t comp = ((uint64_t)e[i] << 32) | (uint64_t)(~j);
                         wmin = min(wmin, e[i]);
-                        if (slot < (uint32_t)p.win_cap) {
-                            if (CLUSTER) dsmem_st64(win_addr + 8u * slot, comp);
-                            else win[slot] = comp;
-                        }
+                        if (slot < (uint32_t)p.win_cap) win[slot] = comp;
                         ++slot;
                     }
                 }
@@ -991,10 +1204,7 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
         }
     }
     wmin = __reduce_min_sync(kFull, wmin);
-    if (lane == 0 && wmin != kFull) {
-        if (CLUSTER) dsmem_red_min(dsmem_addr(&ctrl.wmin, g0), wmin);
-        else atomicMin(&ctrl.wmin, wmin);
-    }
+    if (lane == 0 && wmin != kFull) atomicMin(&ctrl.wmin, wmin);
 
     // ---- a7 (off the plateau): ties in index order, per-warp bases from
     //      the counts above; each warp starts at its first tie ------------ //
@@ -1044,22 +1254,738 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_ragged_kerne
         }
     }
 
-    // ---- a8+a9: the leader sorts the winners and writes the row ----------- //
-    if (CLUSTER) {
-        cluster_sync();   // B3: every winner is in its leader's list
-        if (!leader) return;
-    } else {
-        __syncthreads();
-    }
+    // ---- a8+a9: sort the winners and write the row ---------------------- //
+    __syncthreads();
     const uint32_t n_win = ctrl.win_count;
     if (n_win != n_gt || n_gt > (uint32_t)p.win_cap) {
         if (tid == 0) atomicOr(&g_status, TOPK_DEV_INTERNAL);
     }
     const uint32_t n_sort = n_gt < (uint32_t)p.win_cap ? n_gt : (uint32_t)p.win_cap;
     if (n_sort > 0) {
-        const uint32_t kmax = CLUSTER ? ctrl.kmax_tot : ctrl.kmax;
-        sort_and_write<THREADS>(win, reinterpret_cast<uint64_t *>(keys), (int)n_sort, p.win_cap,
-                                ctrl.wmin, kmax, hist, ctrl.scan64, oi, ov, idx_offset);
+        sort_and_write<THREADS>(win, reinterpret_cast<uint64_t *>(keys), (int)n_sort, (int)n_sort, p.win_cap,
+                                ctrl.wmin, ctrl.kmax, hist, ctrl.scan64, oi, ov, idx_offset);
+    }
+    pad_out(oi, ov, (int)k_eff, p.k);
+}
+
+// ------------------------------------------------------------------------- //
+// The cluster kernel: each cluster of CS CTAs takes a group of rows
+// (assign_rows) and every row is worked on by a contiguous group of the
+// cluster's CTAs; the group's first CTA is the row's leader, which sorts the
+// row's candidates and writes it.
+//
+//   1. Each CTA starts bulk copies (TMA) of its whole staged slice into
+//      shared memory, so every byte of the batch is in flight at once.
+//   2. Level 0: one pass over the slice turns scores into order keys in
+//      place and builds the 11-bit top-digit histogram.  After a cluster
+//      barrier every CTA of the group pulls its peers' histograms over DSMEM
+//      and runs the same threshold search, so all of them hold the same
+//      exact integers without a round trip through the leader.
+//   3. The row then either
+//        * is on the +0.0 plateau (the boundary bin holds only +0.0), or
+//        * has few enough entries at or above the boundary bin to sort
+//          them all (candidates: every key >= the bin's lower bound), or
+//        * refines the boundary bin by the next 11 bits (level 1) and,
+//          if still too many, the last 10 bits (level 2), which gives the
+//          exact k-th key T.
+//      The histograms of consecutive levels live in different buffers,
+//      so one cluster barrier per level is enough.
+//   4. Compaction: candidates go to the CTA's own list with shared-memory
+//      atomics (any order: the sort makes it canonical); the CTA then
+//      copies its list into the leader's with one DSMEM store per entry.
+//      With an exact T the entries equal to T are ties: the first r of
+//      them in index order go straight to output positions n_gt + ordinal.
+//   5. After the last cluster barrier the leader sorts the candidates and
+//      writes the row.
+// Every CTA of the cluster runs the same four cluster barriers whatever
+// its row needs.
+// ------------------------------------------------------------------------- //
+struct __align__(16) CCtrl {
+    uint64_t bar;          // completion of the slice's bulk copies
+    uint32_t zeros;        // this CTA's count of exact +0.0 keys
+    uint32_t win_local;    // entries in this CTA's own candidate list
+    uint32_t win_peer;     // leader: entries copied in by the group's other CTAs
+    uint32_t wmin;         // smallest candidate key (leader: of the group)
+    uint32_t wmax;         // largest candidate key (leader: of the group)
+    uint32_t peer_base;    // a peer's slot range in the leader's list
+    uint32_t sel[4];       // threshold search result: digit, above, in bin
+    uint32_t tot[4];       // group totals: +0.0 count
+    uint32_t warp_zeros[32];
+    uint32_t warp_ties[32];
+    uint32_t scan[36];
+    uint64_t scan64[32];
+};
+
+// Sum of the group's histograms over this thread's BPT bins starting at lo.
+template <int THREADS>
+__device__ __forceinline__ void pull_bins(const uint32_t *h, int lo, uint32_t g0, uint32_t gsize, uint32_t crank,
+                                          uint32_t (&v)[kBins / THREADS])
+{
+    constexpr int BPT = kBins / THREADS;
+    constexpr int kBatch = 4;   // remote loads in flight before they are summed
+    load_bins<THREADS>(h, lo, v);
+    for (uint32_t r0 = g0; r0 < g0 + gsize; r0 += kBatch) {
+        uint32_t w[kBatch][BPT];
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b) {
+            const uint32_t r = r0 + (uint32_t)b;
+            if (r < g0 + gsize && r != crank) {
+                dsmem_ld_bins(dsmem_addr(h + lo, r), w[b]);
+            } else {
+#pragma unroll
+                for (int i = 0; i < BPT; ++i) w[b][i] = 0u;
+            }
+        }
+#pragma unroll
+        for (int b = 0; b < kBatch; ++b)
+#pragma unroll
+            for (int i = 0; i < BPT; ++i) v[i] += w[b][i];
+    }
+}
+
+// Threshold search on bins already in registers (see find_bin).
+template <int THREADS>
+__device__ __forceinline__ bool find_bin_v(const uint32_t (&v)[kBins / THREADS], int lo, uint32_t r, uint32_t *sm,
+                                           uint32_t &digit, uint32_t &gt, uint32_t &cnt)
+{
+    constexpr int BPT = kBins / THREADS;
+    uint32_t sum = 0;
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) sum += v[i];
+    const uint32_t incl = block_incl_scan<THREADS>(sum, sm);
+    const uint32_t excl = incl - sum;
+    bool mine = false;
+    if (excl < r && r <= incl) {
+        uint32_t acc = excl;
+#pragma unroll
+        for (int i = BPT - 1; i >= 0; --i) {
+            if (!mine && acc + v[i] >= r) {
+                mine = true;
+                digit = (uint32_t)(lo + i);
+                gt = acc;
+                cnt = v[i];
+            }
+            acc += v[i];
+        }
+    }
+    return mine;
+}
+
+// Pulls the group's histogram h, finds the bin holding the r-th largest
+// entry and returns (digit, entries above it, entries in it) to every
+// thread.  Ends with a __syncthreads.
+template <int THREADS>
+__device__ __forceinline__ void group_select(CCtrl &ctrl, const uint32_t *h, uint32_t g0, uint32_t gsize,
+                                             uint32_t crank, uint32_t r, uint32_t &d, uint32_t &gt, uint32_t &c)
+{
+    constexpr int BPT = kBins / THREADS;
+    const int lo = kBins - ((int)threadIdx.x + 1) * BPT;   // thread 0 owns the top bins
+    uint32_t v[BPT];
+    pull_bins<THREADS>(h, lo, g0, gsize, crank, v);
+    uint32_t dd, gg, cc;
+    if (find_bin_v<THREADS>(v, lo, r, ctrl.scan, dd, gg, cc)) {
+        ctrl.sel[0] = dd;
+        ctrl.sel[1] = gg;
+        ctrl.sel[2] = cc;
+    }
+    __syncthreads();
+    d = ctrl.sel[0];
+    gt = ctrl.sel[1];
+    c = ctrl.sel[2];
+}
+
+// The slice's quads in index order: an optional partial head quad (0), the
+// full quads [bq0, bq1) cut into one contiguous run per warp, and an
+// optional partial tail quad (nq - 1).  Warp 0 owns the head and the last
+// warp the tail, so warp order is index order and the inner loops need no
+// per-slot masks.
+// Quads per lane in flight in the cluster kernel's passes.
+constexpr int kPassQuads = 2;
+
+struct Parts {
+    int q0, q1;       // this warp's run of full quads
+    int head, tail;   // partial quads this warp owns, or -1
+};
+
+template <int THREADS>
+__device__ __forceinline__ Parts slice_parts(const Slice &s, int warp)
+{
+    constexpr int NW = THREADS / 32;
+    Parts pt;
+    const int n = s.bq1 - s.bq0;
+    const int per = (n + NW - 1) / NW;
+    pt.q0 = s.bq0 + min(n, warp * per);
+    pt.q1 = s.bq0 + min(n, warp * per + per);
+    const int head = s.bq0 > 0 ? 0 : -1;
+    const int tail = (s.nq > s.bq1 && s.nq - 1 != head) ? s.nq - 1 : -1;
+    pt.head = warp == 0 ? head : -1;
+    pt.tail = warp == NW - 1 ? tail : -1;
+    return pt;
+}
+
+__device__ __forceinline__ uint4 to_keys(uint4 raw)
+{
+    return make_uint4(order_key(raw.x), order_key(raw.y), order_key(raw.z), order_key(raw.w));
+}
+
+// A full quad's keys: staged (already keys) or read from global memory.
+__device__ __forceinline__ uint4 body_quad(const Slice &s, const uint4 *keys4, int q)
+{
+    if (q < s.sq) return keys4[q];
+    const float4 f = __ldg(reinterpret_cast<const float4 *>(s.gptr) + q);
+    return make_uint4(order_key(__float_as_uint(f.x)), order_key(__float_as_uint(f.y)),
+                      order_key(__float_as_uint(f.z)), order_key(__float_as_uint(f.w)));
+}
+
+// Runs f(kk, valid) over this warp's full quads, U per lane a round; valid
+// says whether the lane's quad u exists.
+template <int U, class F>
+__device__ __forceinline__ void body_rounds(const Slice &s, const uint4 *keys4, const Parts &pt, F &&f)
+{
+    const int lane = threadIdx.x & 31;
+    for (int qb = pt.q0; qb < pt.q1; qb += 32 * U) {
+        uint4 kk[U];
+        bool ok[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int q = qb + u * 32 + lane;
+            ok[u] = q < pt.q1;
+            kk[u] = ok[u] ? body_quad(s, keys4, q) : make_uint4(0, 0, 0, 0);
+        }
+        f(qb, kk, ok);
+    }
+}
+
+// Level-0 pass: staged scores become keys in place; entries are counted by
+// their top 11 bits, exact +0.0 per warp (about half of a ReLU row) rather
+// than by atomics on one bin.
+template <int THREADS>
+__device__ void level0_pass(CCtrl &ctrl, const Slice &s, uint32_t *keys, const Parts &pt, uint32_t *hist)
+{
+    constexpr int U = kPassQuads;
+    constexpr uint32_t kZ = 0x80000000u;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint4 *keys4 = reinterpret_cast<uint4 *>(keys);
+    uint32_t zeros = 0;
+    auto take = [&](uint32_t e, bool v) {
+        const bool z = e == kZ;
+        zeros += v && z;
+        if (v && !z) atomicAdd(&hist[e >> 21], 1u);
+    };
+    for (int qb = pt.q0; qb < pt.q1; qb += 32 * U) {
+        uint4 kk[U];
+        bool ok[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int q = qb + u * 32 + lane;
+            ok[u] = q < pt.q1;
+            kk[u] = make_uint4(0, 0, 0, 0);
+            if (ok[u]) {
+                if (q < s.sq) {
+                    kk[u] = to_keys(keys4[q]);
+                    keys4[q] = kk[u];
+                } else {
+                    kk[u] = body_quad(s, keys4, q);
+                }
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            take(kk[u].x, ok[u]);
+            take(kk[u].y, ok[u]);
+            take(kk[u].z, ok[u]);
+            take(kk[u].w, ok[u]);
+        }
+    }
+    if (lane == 0) {
+        for (int h = 0; h < 2; ++h) {
+            const int q = h == 0 ? pt.head : pt.tail;
+            if (q < 0) continue;
+            uint32_t m;
+            uint4 kk;
+            if (q < s.sq) {
+                m = quad_mask(s, q);
+                kk = to_keys(keys4[q]);
+                keys4[q] = kk;
+            } else {
+                kk = load_quad_global(s, q, m);
+            }
+            take(kk.x, m & 1u);
+            take(kk.y, (m >> 1) & 1u);
+            take(kk.z, (m >> 2) & 1u);
+            take(kk.w, (m >> 3) & 1u);
+        }
+    }
+    zeros = __reduce_add_sync(kFull, zeros);
+    if (lane == 0) {
+        ctrl.warp_zeros[warp] = zeros;
+        if (zeros) {
+            atomicAdd(&ctrl.zeros, zeros);
+            atomicAdd(&hist[kZ >> 21], zeros);
+        }
+    }
+}
+
+// A partial quad's keys (after level 0) and its valid slots.
+__device__ __forceinline__ uint4 partial_quad(const Slice &s, const uint4 *keys4, int q, uint32_t &m)
+{
+    if (q < s.sq) {
+        m = quad_mask(s, q);
+        return keys4[q];
+    }
+    return load_quad_global(s, q, m);
+}
+
+__device__ __forceinline__ uint32_t quad_max(const uint4 &k)
+{
+    return max(max(k.x, k.y), max(k.z, k.w));
+}
+
+__device__ __forceinline__ uint32_t quad_min(const uint4 &k)
+{
+    return min(min(k.x, k.y), min(k.z, k.w));
+}
+
+// Refinement pass: entries whose key matches `prefix` above bit `pshift`
+// (a key range [plo, phi]) are counted by the digit (key >> dshift) & dmask.
+// A quad is looked at entry by entry only when its range meets [plo, phi].
+template <int THREADS>
+__device__ void level_pass(const Slice &s, const uint32_t *keys, const Parts &pt, uint32_t *hist, uint32_t prefix,
+                           int pshift, int dshift, uint32_t dmask)
+{
+    constexpr int U = kPassQuads;
+    const uint4 *keys4 = reinterpret_cast<const uint4 *>(keys);
+    const uint32_t plo = prefix << pshift, phi = plo | ((1u << pshift) - 1u);
+    auto take = [&](uint32_t e, bool v) {
+        if (v && e >= plo && e <= phi) atomicAdd(&hist[(e >> dshift) & dmask], 1u);
+    };
+    body_rounds<U>(s, keys4, pt, [&](int, const uint4 (&kk)[U], const bool (&ok)[U]) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (ok[u] && quad_max(kk[u]) >= plo && quad_min(kk[u]) <= phi) {
+                take(kk[u].x, true);
+                take(kk[u].y, true);
+                take(kk[u].z, true);
+                take(kk[u].w, true);
+            }
+        }
+    });
+    if ((threadIdx.x & 31) == 0) {
+        for (int h = 0; h < 2; ++h) {
+            const int q = h == 0 ? pt.head : pt.tail;
+            if (q < 0) continue;
+            uint32_t m;
+            const uint4 kk = partial_quad(s, keys4, q, m);
+            take(kk.x, m & 1u);
+            take(kk.y, (m >> 1) & 1u);
+            take(kk.z, (m >> 2) & 1u);
+            take(kk.w, (m >> 3) & 1u);
+        }
+    }
+}
+
+// Compaction.  Candidates (EXACT: key > T; else key >= lo) go to this CTA's
+// own list; with an exact T the ties (key == T) take output positions
+// n_gt + ordinal for ordinals below r, in group-wide index order starting at
+// tie_base.  A count pass gives every warp its base in the list and in the
+// tie order, and a write pass places the entries with warp scans, so the
+// list comes out in index order with no shared counter.  The smallest and
+// largest candidate keys go to ctrl.wmin / ctrl.wmax.  Ends with a
+// __syncthreads; the list length is left in ctrl.win_local.
+template <int THREADS, bool EXACT>
+__device__ void compact_slice(CCtrl &ctrl, const Slice &s, const uint32_t *keys, const Parts &pt, uint64_t *win,
+                              uint32_t wcap, uint32_t lo, uint32_t T, uint32_t tie_base, uint32_t r, uint32_t n_gt,
+                              uint32_t k_eff, int64_t idx_offset, int32_t *oi, float *ov)
+{
+    constexpr int NW = THREADS / 32;
+    constexpr int U = kPassQuads;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint4 *keys4 = reinterpret_cast<const uint4 *>(keys);
+    auto is_cand = [&](uint32_t e) { return EXACT ? e > T : e >= lo; };
+    auto is_tie = [&](uint32_t e) { return EXACT && e == T; };
+
+    // Count pass.
+    uint32_t nc = 0, nt = 0;
+    auto count = [&](uint32_t e, bool v) {
+        nc += v && is_cand(e);
+        nt += v && is_tie(e);
+    };
+    // Candidates and ties are both >= thr: most quads are passed over on
+    // their largest key.
+    const uint32_t thr = EXACT ? T : lo;
+    body_rounds<U>(s, keys4, pt, [&](int, const uint4 (&kk)[U], const bool (&ok)[U]) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (ok[u] && quad_max(kk[u]) >= thr) {
+                count(kk[u].x, true);
+                count(kk[u].y, true);
+                count(kk[u].z, true);
+                count(kk[u].w, true);
+            }
+        }
+    });
+    if (lane == 0) {
+        for (int h = 0; h < 2; ++h) {
+            const int q = h == 0 ? pt.head : pt.tail;
+            if (q < 0) continue;
+            uint32_t m;
+            const uint4 kk = partial_quad(s, keys4, q, m);
+            count(kk.x, m & 1u);
+            count(kk.y, (m >> 1) & 1u);
+            count(kk.z, (m >> 2) & 1u);
+            count(kk.w, (m >> 3) & 1u);
+        }
+    }
+    nc = __reduce_add_sync(kFull, nc);
+    nt = __reduce_add_sync(kFull, nt);
+    if (lane == 0) {
+        ctrl.warp_zeros[warp] = nc;
+        ctrl.warp_ties[warp] = nt;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t c = lane < NW ? ctrl.warp_zeros[lane] : 0u;
+        const uint32_t t = lane < NW ? ctrl.warp_ties[lane] : 0u;
+        const uint32_t ci = warp_incl_scan(c), ti = warp_incl_scan(t);
+        if (lane < NW) {
+            ctrl.warp_zeros[lane] = ci - c;
+            ctrl.warp_ties[lane] = ti - t;
+        }
+        if (lane == 31) ctrl.win_local = ci;
+    }
+    __syncthreads();
+
+    // Write pass.
+    uint32_t cbase = ctrl.warp_zeros[warp], tbase = tie_base + ctrl.warp_ties[warp];
+    uint32_t wmin = kFull, wmax = 0;
+    auto put_cand = [&](uint32_t e, int32_t j, uint32_t slot) {
+        wmin = min(wmin, e);
+        wmax = max(wmax, e);
+        if (slot < wcap) win[slot] = ((uint64_t)e << 32) | (uint64_t)(~(uint32_t)j);
+    };
+    auto put_tie = [&](int32_t j, uint32_t ord) {
+        if (ord < r && n_gt + ord < k_eff) {
+            oi[n_gt + ord] = (int32_t)(idx_offset + j);
+            if (ov) ov[n_gt + ord] = __uint_as_float(key_bits(T));
+        }
+    };
+    // A partial quad of this warp, written by lane 0 at the warp's cursors.
+    auto partial = [&](int q) {
+        uint32_t c = 0, t = 0;
+        if (lane == 0) {
+            uint32_t m;
+            const uint4 kk = partial_quad(s, keys4, q, m);
+            const uint32_t e[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if (!((m >> i) & 1u)) continue;
+                if (is_cand(e[i])) put_cand(e[i], s.jbase + 4 * q + i, cbase + c++);
+                if (is_tie(e[i])) put_tie(s.jbase + 4 * q + i, tbase + t++);
+            }
+        }
+        cbase += __shfl_sync(kFull, c, 0);
+        tbase += __shfl_sync(kFull, t, 0);
+    };
+    if (nc > 0 || (nt > 0 && tbase < r)) {   // warp-uniform
+        if (pt.head >= 0) partial(pt.head);
+        body_rounds<U>(s, keys4, pt, [&](int qb, const uint4 (&kk)[U], const bool (&ok)[U]) {
+            uint32_t cm = 0, tm = 0;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (!(ok[u] && quad_max(kk[u]) >= thr)) continue;
+                const uint32_t e[4] = {kk[u].x, kk[u].y, kk[u].z, kk[u].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    cm |= (uint32_t)is_cand(e[i]) << (4 * u + i);
+                    if (EXACT) tm |= (uint32_t)is_tie(e[i]) << (4 * u + i);
+                }
+            }
+            if (__any_sync(kFull, cm != 0)) {
+                // Candidates: slots by a lane prefix (their order is free).
+                const uint32_t cnt = (uint32_t)__popc(cm);
+                const uint32_t ci = warp_incl_scan(cnt);
+                uint32_t slot = cbase + ci - cnt;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    const uint32_t e[4] = {kk[u].x, kk[u].y, kk[u].z, kk[u].w};
+                    const int32_t j0 = s.jbase + 4 * (qb + u * 32 + lane);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if ((cm >> (4 * u + i)) & 1u) put_cand(e[i], j0 + i, slot++);
+                }
+                cbase += __shfl_sync(kFull, ci, 31);
+            }
+            if (EXACT && __any_sync(kFull, tm != 0)) {
+                // Ties follow index order, which within a round is quad u,
+                // then lane, then slot: counts per u packed a byte each
+                // (at most 128) into one warp scan.
+                uint32_t packed = 0;
+#pragma unroll
+                for (int u = 0; u < U; ++u) packed |= (uint32_t)__popc((tm >> (4 * u)) & 0xFu) << (8 * u);
+                const uint32_t ti = warp_incl_scan(packed);
+                const uint32_t ttot = __shfl_sync(kFull, ti, 31), tex = ti - packed;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    uint32_t ord = tbase + ((tex >> (8 * u)) & 0xFFu);
+                    const int32_t j0 = s.jbase + 4 * (qb + u * 32 + lane);
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if ((tm >> (4 * u + i)) & 1u) put_tie(j0 + i, ord++);
+                    tbase += (ttot >> (8 * u)) & 0xFFu;
+                }
+            }
+        });
+        if (pt.tail >= 0) partial(pt.tail);
+    }
+    wmin = __reduce_min_sync(kFull, wmin);
+    wmax = __reduce_max_sync(kFull, wmax);
+    if (lane == 0 && wmin != kFull) {
+        atomicMin(&ctrl.wmin, wmin);
+        atomicMax(&ctrl.wmax, wmax);
+    }
+    __syncthreads();
+}
+
+// After compaction: a peer reserves a range at the top of the leader's list
+// and copies its own list there; the leader keeps its list at the bottom.
+template <int THREADS>
+__device__ __forceinline__ void send_candidates(CCtrl &ctrl, uint64_t *win, uint32_t wcap, uint32_t g0,
+                                                bool leader)
+{
+    const int tid = threadIdx.x;
+    const uint32_t n = min(ctrl.win_local, wcap);
+    if (leader) return;
+    if (tid == 0) {
+        ctrl.peer_base = n ? dsmem_atom_add(dsmem_addr(&ctrl.win_peer, g0), n) : 0u;
+        if (ctrl.wmin != kFull) {
+            dsmem_red_min(dsmem_addr(&ctrl.wmin, g0), ctrl.wmin);
+            dsmem_red_max(dsmem_addr(&ctrl.wmax, g0), ctrl.wmax);
+        }
+    }
+    __syncthreads();
+    const uint32_t base = ctrl.peer_base;
+    if (base + n > wcap) {
+        if (tid == 0) atomicOr(&g_status, TOPK_DEV_INTERNAL);
+        return;
+    }
+    const uint32_t dst = dsmem_addr(win + (wcap - base - n), g0);
+    for (uint32_t i = tid; i < n; i += THREADS) dsmem_st64(dst + 8u * i, win[i]);
+}
+
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kernel(const Params p)
+{
+    constexpr uint32_t kZeroKey = 0x80000000u;   // order key of +0.0
+    constexpr uint32_t kZeroDigit = kZeroKey >> 21;
+    constexpr uint32_t kChunk = 32768;           // bytes per bulk copy
+    extern __shared__ __align__(16) unsigned char smem[];
+    CCtrl &ctrl = *reinterpret_cast<CCtrl *>(smem);
+    uint32_t *hist0 = reinterpret_cast<uint32_t *>(smem + sizeof(CCtrl));   // levels 0 and 2
+    uint32_t *hist1 = hist0 + kBins;                                          // level 1
+    uint64_t *win = reinterpret_cast<uint64_t *>(smem + p.off_win);
+    uint32_t *keys = reinterpret_cast<uint32_t *>(smem + p.off_keys);
+    const uint32_t wcap = (uint32_t)p.win_cap;   // candidate list capacity (a power of two)
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t crank = cluster_rank(), csize = cluster_size();
+    const RowGroup g = assign_rows<THREADS>(p, crank, csize, hist0, hist1, ctrl.scan);
+    if (g.row < 0) return;   // uniform over the cluster: nothing to select
+    const int row = g.row;
+    const uint32_t g0 = g.g0, gsize = g.gsize, grank = crank - g0;
+    const bool leader = grank == 0;
+
+    // Rows handed out by assign_rows have 0 < L < 2^24 and a valid window.
+    const int64_t rs = g.start;
+    const int32_t L = g.len;
+    const uint32_t k_eff = (uint32_t)(p.k < L ? p.k : L);
+    const int64_t idx_offset = p.offset_mode == TOPK_OFFSET_ROW_START ? rs : 0;
+    int32_t *oi = p.out_idx + (int64_t)row * p.k;
+    float *ov = p.out_val ? p.out_val + (int64_t)row * p.k : nullptr;
+
+    Slice s;
+    {
+        const uint64_t pa = (uint64_t)(uintptr_t)p.scores >> 2;   // element address
+        const int64_t e0 = rs, e1 = rs + L;
+        int64_t a0 = e0 + (int64_t)((4u - (uint32_t)((pa + (uint64_t)e0) & 3u)) & 3u);
+        if (a0 > e1) a0 = e1;
+        const int64_t n4 = (e1 - a0) >> 2;
+        // n4 < 2^22 and gsize <= 16: the products fit 32 bits.
+        const int64_t qlo = (uint32_t)n4 * grank / gsize, qhi = (uint32_t)n4 * (grank + 1) / gsize;
+        const int64_t hb = a0 + 4 * qlo, he = a0 + 4 * qhi;
+        const int64_t glo = grank == 0 ? e0 : hb;
+        const int64_t ghi = grank == gsize - 1 ? e1 : he;
+        const int64_t sbase = hb - ((hb - glo + 3) & ~(int64_t)3);
+        s.gptr = p.scores + sbase;
+        s.off0 = (int32_t)(glo - sbase);
+        s.end = (int32_t)(ghi - sbase);
+        s.bq0 = (int32_t)((hb - sbase) >> 2);
+        s.bq1 = (int32_t)((he - sbase) >> 2);
+        s.nq = (s.end + 3) >> 2;
+        s.sq = s.nq < (p.stage_cap >> 2) ? s.nq : (p.stage_cap >> 2);
+        s.jbase = (int32_t)(sbase - rs);
+    }
+    const Parts pt = slice_parts<THREADS>(s, warp);
+
+    // ---- 1. bulk copies of the staged body; the partial head and tail
+    //         quads are read with plain loads ------------------------------- //
+    const int bq_end = s.bq1 < s.sq ? s.bq1 : s.sq;
+    if (tid == 0) {
+        mbar_init(&ctrl.bar, 1);
+        const uint32_t bytes = bq_end > s.bq0 ? 16u * (uint32_t)(bq_end - s.bq0) : 0u;
+        mbar_arrive_expect_tx(&ctrl.bar, bytes);
+        for (uint32_t off = 0; off < bytes; off += kChunk)
+            bulk_load(reinterpret_cast<unsigned char *>(keys + 4 * s.bq0) + off,
+                      reinterpret_cast<const unsigned char *>(s.gptr + 4 * s.bq0) + off,
+                      bytes - off < kChunk ? bytes - off : kChunk, &ctrl.bar);
+    }
+    {
+        // Staged quads outside the body: at most one head and one tail quad.
+        const int q = tid < 1 ? 0 : s.nq - 1;
+        if (tid < 2 && q < s.sq && (q < s.bq0 || q >= s.bq1)) {
+            const uint32_t m = quad_mask(s, q);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if ((m >> i) & 1u) keys[4 * q + i] = __float_as_uint(__ldg(s.gptr + 4 * q + i));
+        }
+    }
+    for (int b = tid; b < 2 * kBins; b += THREADS) hist0[b] = 0u;
+    if (tid == 0) {
+        ctrl.zeros = 0u;
+        ctrl.win_local = 0u;
+        ctrl.win_peer = 0u;
+        ctrl.wmin = kFull;
+        ctrl.wmax = 0u;
+    }
+    __syncthreads();
+    mbar_wait_bounded(&ctrl.bar, 0);
+
+    // ---- 2. level 0: keys in place, top-digit histogram, +0.0 counts ---- //
+    level0_pass<THREADS>(ctrl, s, keys, pt, hist0);
+    __syncthreads();
+    cluster_sync();   // B0: every CTA's level-0 histogram and counts are final
+
+    if (warp == 0) {
+        // The group's +0.0 count: lane l reads the group's l-th CTA.
+        const uint32_t rk = g0 + (uint32_t)lane;
+        uint32_t z = 0;
+        if (lane < (int)gsize) z = rk == crank ? ctrl.zeros : dsmem_ld(dsmem_addr(&ctrl.zeros, rk));
+        z = __reduce_add_sync(kFull, z);
+        if (lane == 0) ctrl.tot[0] = z;
+    }
+    enum { kRefine = 0, kRange = 1, kExact = 2 };
+    int mode = kRefine;
+    uint32_t r = k_eff, n_gt = 0, prefix = 0, lo_key = 0, T = 0, n_cand = 0;
+    bool plateau = false;
+    {
+        uint32_t d, gt, c;
+        group_select<THREADS>(ctrl, hist0, g0, gsize, crank, r, d, gt, c);
+        if (d == kZeroDigit && c == ctrl.tot[0]) {
+            // The boundary bin holds only +0.0: the k-th key is +0.0.
+            mode = kExact;
+            plateau = true;
+            T = kZeroKey;
+            n_gt = gt;
+            r -= gt;
+        } else if (gt + c <= wcap) {
+            mode = kRange;
+            lo_key = d << 21;
+            n_cand = gt + c;
+        } else {
+            prefix = d;
+            n_gt = gt;
+            r -= gt;
+        }
+    }
+    // Ties before this CTA in the group (plateau: +0.0 entries).
+    auto ties_before = [&](const uint32_t *src) {
+        if (warp == 0) {
+            uint32_t part = lane < (int)grank ? dsmem_ld(dsmem_addr(src, g0 + (uint32_t)lane)) : 0u;
+            part = __reduce_add_sync(kFull, part);
+            if (lane == 0) ctrl.scan[0] = part;
+        }
+        __syncthreads();
+        return ctrl.scan[0];
+    };
+    if (mode != kRefine) {
+        if (plateau)
+            compact_slice<THREADS, true>(ctrl, s, keys, pt, win, wcap, 0u, T, ties_before(&ctrl.zeros), r, n_gt,
+                                         k_eff, idx_offset, oi, ov);
+        else
+            compact_slice<THREADS, false>(ctrl, s, keys, pt, win, wcap, lo_key, 0u, 0u, r, n_gt, k_eff, idx_offset,
+                                          oi, ov);
+        send_candidates<THREADS>(ctrl, win, wcap, g0, leader);
+    } else {
+        level_pass<THREADS>(s, keys, pt, hist1, prefix, 21, 10, 0x7FFu);
+        __syncthreads();
+    }
+    cluster_sync();   // B1
+
+    if (mode == kRefine) {
+        uint32_t d, gt, c;
+        group_select<THREADS>(ctrl, hist1, g0, gsize, crank, r, d, gt, c);
+        if (n_gt + gt + c <= wcap) {
+            mode = kRange;
+            lo_key = (prefix << 21) | (d << 10);
+            n_cand = n_gt + gt + c;
+            compact_slice<THREADS, false>(ctrl, s, keys, pt, win, wcap, lo_key, 0u, 0u, r, n_gt, k_eff,
+                                          idx_offset, oi, ov);
+            send_candidates<THREADS>(ctrl, win, wcap, g0, leader);
+        } else {
+            prefix = (prefix << 11) | d;
+            n_gt += gt;
+            r -= gt;
+            // Every peer pulled hist0 before B1: it can be reused.
+            for (int b = tid; b < kBins; b += THREADS) hist0[b] = 0u;
+            __syncthreads();
+            level_pass<THREADS>(s, keys, pt, hist0, prefix, 10, 0, 0x3FFu);
+            __syncthreads();
+        }
+    }
+    cluster_sync();   // B2
+
+    if (mode == kRefine) {
+        uint32_t d, gt, c;
+        group_select<THREADS>(ctrl, hist0, g0, gsize, crank, r, d, gt, c);
+        mode = kExact;
+        T = (prefix << 10) | d;
+        n_gt += gt;
+        r -= gt;
+        const uint32_t tb = ties_before(&hist0[T & 0x3FFu]);
+        compact_slice<THREADS, true>(ctrl, s, keys, pt, win, wcap, 0u, T, tb, r, n_gt, k_eff, idx_offset, oi, ov);
+        send_candidates<THREADS>(ctrl, win, wcap, g0, leader);
+    }
+    cluster_sync();   // B3: every candidate is in its leader's list
+    if (!leader) return;
+
+    // ---- 5. the leader sorts the candidates and writes the row ---------- //
+    const uint32_t n_local = min(ctrl.win_local, wcap), n_peer = ctrl.win_peer;
+    uint32_t n = n_local + n_peer;
+    const uint32_t expect = mode == kRange ? n_cand : n_gt;
+    if (n != expect || n > wcap) {
+        if (tid == 0) atomicOr(&g_status, TOPK_DEV_INTERNAL);
+        n = min(n, wcap);
+    }
+    // Move the peers' block [wcap - n_peer, wcap) down to follow the
+    // leader's own entries (the destination never overtakes the source).
+    for (uint32_t b = 0; b < n_peer && n_local + n_peer <= wcap; b += 4 * THREADS) {
+        uint64_t t[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t x = b + (uint32_t)i * THREADS + tid;
+            t[i] = x < n_peer ? win[wcap - n_peer + x] : 0ull;
+        }
+        __syncthreads();
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uint32_t x = b + (uint32_t)i * THREADS + tid;
+            if (x < n_peer) win[n_local + x] = t[i];
+        }
+        __syncthreads();
+    }
+    const uint32_t n_out = mode == kRange ? k_eff : n_gt;
+    if (n > 0) {
+        sort_and_write<THREADS>(win, reinterpret_cast<uint64_t *>(keys), (int)n, (int)min(n, n_out), (int)wcap,
+                                ctrl.wmin, ctrl.wmax, hist0, ctrl.scan64, oi, ov, idx_offset);
     }
     pad_out(oi, ov, (int)k_eff, p.k);
 }
@@ -1076,9 +2002,9 @@ struct Variant {
 };
 
 const Variant kVariants[] = {
-    {topk_ragged_kernel<256, false>, 256, false},
-    {topk_ragged_kernel<512, true>, 512, true},
-    {topk_ragged_kernel<1024, true>, 1024, true},
+    {topk_row_kernel<256>, 256, false},
+    {topk_cluster_kernel<512>, 512, true},
+    {topk_cluster_kernel<1024>, 1024, true},
 };
 
 struct DeviceInfo {
@@ -1097,7 +2023,6 @@ DeviceInfo g_devices[kMaxDevices];
 struct Plan {
     const Variant *v;
     int cluster;
-    int grouped;
     int stage_cap;
     int win_cap;
     int off_win, off_keys, smem;
@@ -1113,55 +2038,70 @@ int next_pow2(int x)
 
 int header_bytes(bool cluster)
 {
-    return (int)sizeof(Ctrl) + kBins * 4 * (cluster ? 2 : 1);
+    return cluster ? (int)sizeof(CCtrl) + 2 * kBins * 4 : (int)sizeof(Ctrl) + kBins * 4;
+}
+
+// Candidate slots: the one-CTA kernel keeps the winners (fewer than k); the
+// cluster kernel's leader keeps up to twice k candidates, so that most rows
+// can be sorted after one or two histogram levels.
+int list_cap(bool cluster, int k)
+{
+    return cluster ? 2 * next_pow2(k) : next_pow2(k - 1 > 1 ? k - 1 : 1);
 }
 
 // Launch shape from the host arguments alone (row lengths live on the
 // device and are never read here).
 //   * B >= 4 x SMs: one 256-thread CTA per row, several CTAs per SM.
-//   * B x 16 <= SMs: a 16-CTA cluster of 1024-thread CTAs per row, each CTA
-//     with all of an SM's shared memory (very long rows stage the most).
-//   * otherwise: one resident wave of G clusters of CS 512-thread CTAs (two
-//     per SM); the clusters share out the rows by length and each cluster
-//     deals its CTAs to its rows in proportion to their lengths
-//     (assign_rows), so every CTA gets a similar slice.
+//   * otherwise one resident wave of G clusters of CS CTAs, either
+//     1024-thread CTAs with all of an SM's shared memory or 512-thread CTAs
+//     two to an SM; the clusters share out the rows by length and each
+//     cluster deals its CTAs to its rows so that the largest slice is as
+//     small as possible (assign_rows).  Of the shapes that give every row a
+//     CTA, the planner takes the one whose typical row gets the most staging
+//     capacity, min(CS, G x CS / B) x scores staged per CTA, and on a tie the
+//     one with more CTAs.
 //   * batches too large for that wave fall back to one CTA per row.
 // Each CTA stages what shared memory allows and re-reads the rest of its
 // slice from L2.
+int stage_cap_for(int smem_budget, int off_keys)
+{
+    return ((smem_budget - off_keys) / 4) & ~127;
+}
+
 Plan make_plan(int32_t B, int32_t k, const DeviceInfo &dev)
 {
     Plan pl{};
-    pl.win_cap = next_pow2(k - 1 > 1 ? k - 1 : 1);
     const int sms = dev.sm_count;
+    // The staged keys are read as 16-byte vectors: keep them 128-byte aligned
+    // whatever the winner array's size (k <= 2 gives a single 8-byte slot).
+    const int off_keys_cluster = (header_bytes(true) + list_cap(true, k) * 8 + 127) & ~127;
     int vi = 0, cluster = 1, smem_budget = 0, grid = B;
-    pl.grouped = 0;
     if (B < 4 * sms) {
-        if ((int64_t)B * 16 <= sms && dev.max_clusters[2][16] > 0) {
-            vi = 2;
-            cluster = 16;
-            smem_budget = dev.max_smem;
-            grid = B * 16;
-        } else {
-            for (int cs = 16; cs >= 2; cs /= 2) {
-                const int g = min(2 * sms / cs, dev.max_clusters[1][cs]);
-                if (g > 0 && (int64_t)g * cs >= B) {
-                    vi = 1;
+        double best = 0.0;
+        for (int v = 2; v >= 1; --v) {
+            const int budget = v == 2 ? dev.max_smem : dev.smem_per_sm / 2 - 1024;
+            const int cap = stage_cap_for(budget, off_keys_cluster);
+            for (int cs = 2; cs <= 16; cs *= 2) {
+                int g = dev.max_clusters[v][cs];
+                if (v == 1) g = min(g, 2 * sms / cs);
+                if (g <= 0 || (int64_t)g * cs < B || cap <= 0) continue;
+                const double share = min((double)cs, (double)g * cs / B) * cap;
+                if (share > best * 1.0001 || (share > best * 0.9999 && g * cs > grid)) {
+                    best = share;
+                    vi = v;
                     cluster = cs;
-                    smem_budget = dev.smem_per_sm / 2 - 1024;
+                    smem_budget = budget;
                     grid = g * cs;
-                    pl.grouped = 1;
-                    break;
                 }
             }
         }
     }
     pl.v = &kVariants[vi];
     pl.cluster = cluster;
+    pl.win_cap = list_cap(pl.v->cluster, k);
     pl.off_win = header_bytes(pl.v->cluster);
-    // The staged keys are read as 16-byte vectors: keep them 128-byte aligned
-    // whatever the winner array's size (k <= 2 gives a single 8-byte slot).
     pl.off_keys = (pl.off_win + pl.win_cap * 8 + 127) & ~127;
-    int stage_cap = smem_budget > 0 ? ((smem_budget - pl.off_keys) / 4) & ~127 : 4096 + 256;
+    int stage_cap = smem_budget > 0 ? stage_cap_for(smem_budget, pl.off_keys) : 4096 + 256;
     // The staging area doubles as the sort's second buffer after compaction.
     if (stage_cap < 2 * pl.win_cap) stage_cap = 2 * pl.win_cap;
     pl.stage_cap = stage_cap;
@@ -1334,7 +2274,6 @@ int topk_ragged(const float *scores, int64_t n_scores, const int32_t *row_starts
     prm.win_cap = pl.win_cap;
     prm.off_win = pl.off_win;
     prm.off_keys = pl.off_keys;
-    prm.grouped = pl.grouped;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)pl.grid, 1, 1);

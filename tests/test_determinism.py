@@ -85,8 +85,11 @@ def test_batch_composition_invariance():
 
 def test_launch_shapes_cover_all_variants():
     shapes = {B: pkg.launch_info(B, 2048) for B in (1, 4, 64, 300, 400, 4096)}
-    assert shapes[4]["cluster"] == 16 and shapes[4]["threads"] == 1024
-    assert shapes[64]["threads"] == 512 and shapes[64]["cluster"] >= 2
+    kinds = {(info["threads"], info["cluster"] > 1) for info in shapes.values()}
+    # 1024-thread clusters, 512-thread clusters (two CTAs per SM) and one
+    # 256-thread CTA per row are all reached by some batch size.
+    assert {(1024, True), (512, True), (256, False)} <= kinds, shapes
+    assert shapes[4]["cluster"] == 16
     assert shapes[4096]["cluster"] == 1 and shapes[4096]["grid"] == 4096
     for info in shapes.values():
         assert info["launches"] == 1
