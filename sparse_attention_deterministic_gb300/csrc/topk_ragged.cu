@@ -140,28 +140,6 @@ __device__ __forceinline__ uint32_t dsmem_addr(const void *p, uint32_t rank)
     return remote;
 }
 
-__device__ __forceinline__ uint32_t dsmem_atom_add(uint32_t addr, uint32_t v)
-{
-    uint32_t old;
-    asm volatile("atom.shared::cluster.add.u32 %0, [%1], %2;" : "=r"(old) : "r"(addr), "r"(v) : "memory");
-    return old;
-}
-
-__device__ __forceinline__ void dsmem_st64(uint32_t addr, uint64_t v)
-{
-    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
-}
-
-__device__ __forceinline__ void dsmem_red_max(uint32_t addr, uint32_t v)
-{
-    asm volatile("red.shared::cluster.max.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
-__device__ __forceinline__ void dsmem_red_min(uint32_t addr, uint32_t v)
-{
-    asm volatile("red.shared::cluster.min.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
-}
-
 __device__ __forceinline__ uint32_t dsmem_ld(uint32_t addr)
 {
     uint32_t v;
@@ -1290,24 +1268,21 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_row_kernel(c
 //          exact k-th key T.
 //      The histograms of consecutive levels live in different buffers,
 //      so one cluster barrier per level is enough.
-//   4. Compaction: candidates go to the CTA's own list with shared-memory
-//      atomics (any order: the sort makes it canonical); the CTA then
-//      copies its list into the leader's with one DSMEM store per entry.
-//      With an exact T the entries equal to T are ties: the first r of
-//      them in index order go straight to output positions n_gt + ordinal.
-//   5. After the last cluster barrier the leader sorts the candidates and
-//      writes the row.
+//   4. Compaction: candidates go to the CTA's own list.  With an exact T
+//      the entries equal to T are ties: the first r of them in index order
+//      go straight to output positions n_gt + ordinal.
+//   5. After the last level barrier the leader pulls the group's lists into
+//      its staging area over DSMEM, releases the peers (a split cluster
+//      barrier) and sorts the candidates and writes the row.
 // Every CTA of the cluster runs the same four cluster barriers whatever
 // its row needs.
 // ------------------------------------------------------------------------- //
 struct __align__(16) CCtrl {
     uint64_t bar;          // completion of the slice's bulk copies
     uint32_t zeros;        // this CTA's count of exact +0.0 keys
-    uint32_t win_local;    // entries in this CTA's own candidate list
-    uint32_t win_peer;     // leader: entries copied in by the group's other CTAs
-    uint32_t wmin;         // smallest candidate key (leader: of the group)
-    uint32_t wmax;         // largest candidate key (leader: of the group)
-    uint32_t peer_base;    // a peer's slot range in the leader's list
+    uint32_t win_local;    // entries in this CTA's candidate list
+    uint32_t wmin;         // smallest candidate key in this CTA's list
+    uint32_t wmax;         // largest candidate key in this CTA's list
     uint32_t sel[4];       // threshold search result: digit, above, in bin
     uint32_t tot[4];       // group totals: +0.0 count
     uint32_t warp_zeros[32];
@@ -1423,6 +1398,23 @@ __device__ __forceinline__ Parts slice_parts(const Slice &s, int warp)
     return pt;
 }
 
+// A fully staged slice (every quad in shared memory) whose partial end
+// quads hold the sentinel key 0 in their empty slots: every warp takes a
+// contiguous run of all nq quads and there are no separate partial quads.
+// Level 0 counts the sentinels into bin 0 and takes them out again; the
+// later passes use it only when their key range excludes 0.
+template <int THREADS>
+__device__ __forceinline__ Parts staged_parts(const Slice &s, int warp)
+{
+    const WarpSeg w = warp_segment<THREADS>(s.nq, warp);
+    Parts pt;
+    pt.q0 = w.q0;
+    pt.q1 = w.q1;
+    pt.head = -1;
+    pt.tail = -1;
+    return pt;
+}
+
 __device__ __forceinline__ uint4 to_keys(uint4 raw)
 {
     return make_uint4(order_key(raw.x), order_key(raw.y), order_key(raw.z), order_key(raw.w));
@@ -1438,8 +1430,9 @@ __device__ __forceinline__ uint4 body_quad(const Slice &s, const uint4 *keys4, i
 }
 
 // Runs f(kk, valid) over this warp's full quads, U per lane a round; valid
-// says whether the lane's quad u exists.
-template <int U, class F>
+// says whether the lane's quad u exists.  STAGED: every quad is in shared
+// memory.
+template <int U, bool STAGED, class F>
 __device__ __forceinline__ void body_rounds(const Slice &s, const uint4 *keys4, const Parts &pt, F &&f)
 {
     const int lane = threadIdx.x & 31;
@@ -1450,7 +1443,8 @@ __device__ __forceinline__ void body_rounds(const Slice &s, const uint4 *keys4, 
         for (int u = 0; u < U; ++u) {
             const int q = qb + u * 32 + lane;
             ok[u] = q < pt.q1;
-            kk[u] = ok[u] ? body_quad(s, keys4, q) : make_uint4(0, 0, 0, 0);
+            kk[u] = make_uint4(0, 0, 0, 0);
+            if (ok[u]) kk[u] = STAGED ? keys4[q] : body_quad(s, keys4, q);
         }
         f(qb, kk, ok);
     }
@@ -1459,8 +1453,9 @@ __device__ __forceinline__ void body_rounds(const Slice &s, const uint4 *keys4, 
 // Level-0 pass: staged scores become keys in place; entries are counted by
 // their top 11 bits, exact +0.0 per warp (about half of a ReLU row) rather
 // than by atomics on one bin.
-template <int THREADS>
-__device__ void level0_pass(CCtrl &ctrl, const Slice &s, uint32_t *keys, const Parts &pt, uint32_t *hist)
+template <int THREADS, bool STAGED>
+__device__ void level0_pass(CCtrl &ctrl, const Slice &s, uint32_t *keys, const Parts &pt, uint32_t *hist,
+                            uint32_t n_sentinel)
 {
     constexpr int U = kPassQuads;
     constexpr uint32_t kZ = 0x80000000u;
@@ -1481,7 +1476,7 @@ __device__ void level0_pass(CCtrl &ctrl, const Slice &s, uint32_t *keys, const P
             ok[u] = q < pt.q1;
             kk[u] = make_uint4(0, 0, 0, 0);
             if (ok[u]) {
-                if (q < s.sq) {
+                if (STAGED || q < s.sq) {
                     kk[u] = to_keys(keys4[q]);
                     keys4[q] = kk[u];
                 } else {
@@ -1524,6 +1519,7 @@ __device__ void level0_pass(CCtrl &ctrl, const Slice &s, uint32_t *keys, const P
             atomicAdd(&hist[kZ >> 21], zeros);
         }
     }
+    if (STAGED && threadIdx.x == 0 && n_sentinel) atomicSub(&hist[0], n_sentinel);
 }
 
 // A partial quad's keys (after level 0) and its valid slots.
@@ -1549,7 +1545,7 @@ __device__ __forceinline__ uint32_t quad_min(const uint4 &k)
 // Refinement pass: entries whose key matches `prefix` above bit `pshift`
 // (a key range [plo, phi]) are counted by the digit (key >> dshift) & dmask.
 // A quad is looked at entry by entry only when its range meets [plo, phi].
-template <int THREADS>
+template <int THREADS, bool STAGED>
 __device__ void level_pass(const Slice &s, const uint32_t *keys, const Parts &pt, uint32_t *hist, uint32_t prefix,
                            int pshift, int dshift, uint32_t dmask)
 {
@@ -1559,7 +1555,7 @@ __device__ void level_pass(const Slice &s, const uint32_t *keys, const Parts &pt
     auto take = [&](uint32_t e, bool v) {
         if (v && e >= plo && e <= phi) atomicAdd(&hist[(e >> dshift) & dmask], 1u);
     };
-    body_rounds<U>(s, keys4, pt, [&](int, const uint4 (&kk)[U], const bool (&ok)[U]) {
+    body_rounds<U, STAGED>(s, keys4, pt, [&](int, const uint4 (&kk)[U], const bool (&ok)[U]) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (ok[u] && quad_max(kk[u]) >= plo && quad_min(kk[u]) <= phi) {
@@ -1592,7 +1588,7 @@ __device__ void level_pass(const Slice &s, const uint32_t *keys, const Parts &pt
 // list comes out in index order with no shared counter.  The smallest and
 // largest candidate keys go to ctrl.wmin / ctrl.wmax.  Ends with a
 // __syncthreads; the list length is left in ctrl.win_local.
-template <int THREADS, bool EXACT>
+template <int THREADS, bool EXACT, bool STAGED>
 __device__ void compact_slice(CCtrl &ctrl, const Slice &s, const uint32_t *keys, const Parts &pt, uint64_t *win,
                               uint32_t wcap, uint32_t lo, uint32_t T, uint32_t tie_base, uint32_t r, uint32_t n_gt,
                               uint32_t k_eff, int64_t idx_offset, int32_t *oi, float *ov)
@@ -1613,7 +1609,7 @@ __device__ void compact_slice(CCtrl &ctrl, const Slice &s, const uint32_t *keys,
     // Candidates and ties are both >= thr: most quads are passed over on
     // their largest key.
     const uint32_t thr = EXACT ? T : lo;
-    body_rounds<U>(s, keys4, pt, [&](int, const uint4 (&kk)[U], const bool (&ok)[U]) {
+    body_rounds<U, STAGED>(s, keys4, pt, [&](int, const uint4 (&kk)[U], const bool (&ok)[U]) {
 #pragma unroll
         for (int u = 0; u < U; ++u) {
             if (ok[u] && quad_max(kk[u]) >= thr) {
@@ -1688,7 +1684,7 @@ __device__ void compact_slice(CCtrl &ctrl, const Slice &s, const uint32_t *keys,
     };
     if (nc > 0 || (nt > 0 && tbase < r)) {   // warp-uniform
         if (pt.head >= 0) partial(pt.head);
-        body_rounds<U>(s, keys4, pt, [&](int qb, const uint4 (&kk)[U], const bool (&ok)[U]) {
+        body_rounds<U, STAGED>(s, keys4, pt, [&](int qb, const uint4 (&kk)[U], const bool (&ok)[U]) {
             uint32_t cm = 0, tm = 0;
 #pragma unroll
             for (int u = 0; u < U; ++u) {
@@ -1746,30 +1742,37 @@ __device__ void compact_slice(CCtrl &ctrl, const Slice &s, const uint32_t *keys,
     __syncthreads();
 }
 
-// After compaction: a peer reserves a range at the top of the leader's list
-// and copies its own list there; the leader keeps its list at the bottom.
-template <int THREADS>
-__device__ __forceinline__ void send_candidates(CCtrl &ctrl, uint64_t *win, uint32_t wcap, uint32_t g0,
-                                                bool leader)
+__device__ __forceinline__ uint64_t dsmem_ld64(uint32_t addr)
 {
-    const int tid = threadIdx.x;
-    const uint32_t n = min(ctrl.win_local, wcap);
-    if (leader) return;
-    if (tid == 0) {
-        ctrl.peer_base = n ? dsmem_atom_add(dsmem_addr(&ctrl.win_peer, g0), n) : 0u;
-        if (ctrl.wmin != kFull) {
-            dsmem_red_min(dsmem_addr(&ctrl.wmin, g0), ctrl.wmin);
-            dsmem_red_max(dsmem_addr(&ctrl.wmax, g0), ctrl.wmax);
-        }
-    }
-    __syncthreads();
-    const uint32_t base = ctrl.peer_base;
-    if (base + n > wcap) {
-        if (tid == 0) atomicOr(&g_status, TOPK_DEV_INTERNAL);
-        return;
-    }
-    const uint32_t dst = dsmem_addr(win + (wcap - base - n), g0);
-    for (uint32_t i = tid; i < n; i += THREADS) dsmem_st64(dst + 8u * i, win[i]);
+    uint64_t v;
+    asm volatile("ld.shared::cluster.u64 %0, [%1];" : "=l"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+// The staged (mask-free) passes serve when their key range excludes the
+// sentinel key 0; otherwise, or for a slice not wholly staged, the masked
+// passes run on the slice's own parts.
+template <int THREADS>
+__device__ __forceinline__ void refine_pass(bool staged, const Slice &s, const uint32_t *keys, const Parts &pt,
+                                            const Parts &ptm, uint32_t *hist, uint32_t prefix, int pshift, int dshift,
+                                            uint32_t dmask)
+{
+    if (staged && prefix != 0u) level_pass<THREADS, true>(s, keys, pt, hist, prefix, pshift, dshift, dmask);
+    else level_pass<THREADS, false>(s, keys, ptm, hist, prefix, pshift, dshift, dmask);
+}
+
+template <int THREADS, bool EXACT>
+__device__ __forceinline__ void compact(bool staged, CCtrl &ctrl, const Slice &s, const uint32_t *keys,
+                                        const Parts &pt, const Parts &ptm, uint64_t *win, uint32_t wcap, uint32_t lo,
+                                        uint32_t T, uint32_t tie_base, uint32_t r, uint32_t n_gt, uint32_t k_eff,
+                                        int64_t idx_offset, int32_t *oi, float *ov)
+{
+    if (staged && (EXACT ? T != 0u : lo != 0u))
+        compact_slice<THREADS, EXACT, true>(ctrl, s, keys, pt, win, wcap, lo, T, tie_base, r, n_gt, k_eff, idx_offset,
+                                            oi, ov);
+    else
+        compact_slice<THREADS, EXACT, false>(ctrl, s, keys, ptm, win, wcap, lo, T, tie_base, r, n_gt, k_eff,
+                                             idx_offset, oi, ov);
 }
 
 template <int THREADS>
@@ -1824,7 +1827,13 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
         s.sq = s.nq < (p.stage_cap >> 2) ? s.nq : (p.stage_cap >> 2);
         s.jbase = (int32_t)(sbase - rs);
     }
-    const Parts pt = slice_parts<THREADS>(s, warp);
+    // A slice held entirely in shared memory runs the passes mask-free
+    // (staged_parts); otherwise the full quads, the partial end quads and
+    // the part beyond the staging area are read as they lie.
+    const bool staged = s.sq == s.nq;   // CTA-uniform
+    const Parts pt = staged ? staged_parts<THREADS>(s, warp) : slice_parts<THREADS>(s, warp);
+    const Parts ptm = slice_parts<THREADS>(s, warp);   // masked parts (key-0 ranges)
+    const uint32_t n_sentinel = (uint32_t)(4 * s.nq - (s.end - s.off0));
 
     // ---- 1. bulk copies of the staged body; the partial head and tail
     //         quads are read with plain loads ------------------------------- //
@@ -1842,17 +1851,17 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
         // Staged quads outside the body: at most one head and one tail quad.
         const int q = tid < 1 ? 0 : s.nq - 1;
         if (tid < 2 && q < s.sq && (q < s.bq0 || q >= s.bq1)) {
+            // Empty slots get raw bits 0xFFFFFFFF, whose order key is 0.
             const uint32_t m = quad_mask(s, q);
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                if ((m >> i) & 1u) keys[4 * q + i] = __float_as_uint(__ldg(s.gptr + 4 * q + i));
+                keys[4 * q + i] = ((m >> i) & 1u) ? __float_as_uint(__ldg(s.gptr + 4 * q + i)) : kFull;
         }
     }
     for (int b = tid; b < 2 * kBins; b += THREADS) hist0[b] = 0u;
     if (tid == 0) {
         ctrl.zeros = 0u;
         ctrl.win_local = 0u;
-        ctrl.win_peer = 0u;
         ctrl.wmin = kFull;
         ctrl.wmax = 0u;
     }
@@ -1860,7 +1869,8 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
     mbar_wait_bounded(&ctrl.bar, 0);
 
     // ---- 2. level 0: keys in place, top-digit histogram, +0.0 counts ---- //
-    level0_pass<THREADS>(ctrl, s, keys, pt, hist0);
+    if (staged) level0_pass<THREADS, true>(ctrl, s, keys, pt, hist0, n_sentinel);
+    else level0_pass<THREADS, false>(ctrl, s, keys, pt, hist0, 0u);
     __syncthreads();
     cluster_sync();   // B0: every CTA's level-0 histogram and counts are final
 
@@ -1908,14 +1918,13 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
     };
     if (mode != kRefine) {
         if (plateau)
-            compact_slice<THREADS, true>(ctrl, s, keys, pt, win, wcap, 0u, T, ties_before(&ctrl.zeros), r, n_gt,
-                                         k_eff, idx_offset, oi, ov);
+            compact<THREADS, true>(staged, ctrl, s, keys, pt, ptm, win, wcap, 0u, T, ties_before(&ctrl.zeros), r,
+                                   n_gt, k_eff, idx_offset, oi, ov);
         else
-            compact_slice<THREADS, false>(ctrl, s, keys, pt, win, wcap, lo_key, 0u, 0u, r, n_gt, k_eff, idx_offset,
-                                          oi, ov);
-        send_candidates<THREADS>(ctrl, win, wcap, g0, leader);
+            compact<THREADS, false>(staged, ctrl, s, keys, pt, ptm, win, wcap, lo_key, 0u, 0u, r, n_gt, k_eff,
+                                    idx_offset, oi, ov);
     } else {
-        level_pass<THREADS>(s, keys, pt, hist1, prefix, 21, 10, 0x7FFu);
+        refine_pass<THREADS>(staged, s, keys, pt, ptm, hist1, prefix, 21, 10, 0x7FFu);
         __syncthreads();
     }
     cluster_sync();   // B1
@@ -1927,17 +1936,16 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
             mode = kRange;
             lo_key = (prefix << 21) | (d << 10);
             n_cand = n_gt + gt + c;
-            compact_slice<THREADS, false>(ctrl, s, keys, pt, win, wcap, lo_key, 0u, 0u, r, n_gt, k_eff,
-                                          idx_offset, oi, ov);
-            send_candidates<THREADS>(ctrl, win, wcap, g0, leader);
-        } else {
+            compact<THREADS, false>(staged, ctrl, s, keys, pt, ptm, win, wcap, lo_key, 0u, 0u, r, n_gt, k_eff,
+                                    idx_offset, oi, ov);
+            } else {
             prefix = (prefix << 11) | d;
             n_gt += gt;
             r -= gt;
             // Every peer pulled hist0 before B1: it can be reused.
             for (int b = tid; b < kBins; b += THREADS) hist0[b] = 0u;
             __syncthreads();
-            level_pass<THREADS>(s, keys, pt, hist0, prefix, 10, 0, 0x3FFu);
+            refine_pass<THREADS>(staged, s, keys, pt, ptm, hist0, prefix, 10, 0, 0x3FFu);
             __syncthreads();
         }
     }
@@ -1951,43 +1959,66 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
         n_gt += gt;
         r -= gt;
         const uint32_t tb = ties_before(&hist0[T & 0x3FFu]);
-        compact_slice<THREADS, true>(ctrl, s, keys, pt, win, wcap, 0u, T, tb, r, n_gt, k_eff, idx_offset, oi, ov);
-        send_candidates<THREADS>(ctrl, win, wcap, g0, leader);
+        compact<THREADS, true>(staged, ctrl, s, keys, pt, ptm, win, wcap, 0u, T, tb, r, n_gt, k_eff, idx_offset, oi,
+                               ov);
     }
-    cluster_sync();   // B3: every candidate is in its leader's list
-    if (!leader) return;
+    cluster_sync();   // B3: every CTA's candidate list is final
 
-    // ---- 5. the leader sorts the candidates and writes the row ---------- //
-    const uint32_t n_local = min(ctrl.win_local, wcap), n_peer = ctrl.win_peer;
-    uint32_t n = n_local + n_peer;
-    const uint32_t expect = mode == kRange ? n_cand : n_gt;
-    if (n != expect || n > wcap) {
-        if (tid == 0) atomicOr(&g_status, TOPK_DEV_INTERNAL);
-        n = min(n, wcap);
-    }
-    // Move the peers' block [wcap - n_peer, wcap) down to follow the
-    // leader's own entries (the destination never overtakes the source).
-    for (uint32_t b = 0; b < n_peer && n_local + n_peer <= wcap; b += 4 * THREADS) {
-        uint64_t t[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t x = b + (uint32_t)i * THREADS + tid;
-            t[i] = x < n_peer ? win[wcap - n_peer + x] : 0ull;
+    // ---- 5. the leader gathers the group's lists into its staging area
+    //         (its own keys are no longer needed), releases the peers and
+    //         sorts; the peers wait until it has read their lists ---------- //
+    uint64_t *cand = reinterpret_cast<uint64_t *>(keys);
+    uint32_t n = 0;
+    if (leader) {
+        if (warp == 0) {
+            const uint32_t rk = g0 + (uint32_t)lane;
+            uint32_t cnt = 0, mn = kFull, mx = 0;
+            if (lane < (int)gsize) {
+                cnt = rk == crank ? ctrl.win_local : dsmem_ld(dsmem_addr(&ctrl.win_local, rk));
+                mn = rk == crank ? ctrl.wmin : dsmem_ld(dsmem_addr(&ctrl.wmin, rk));
+                mx = rk == crank ? ctrl.wmax : dsmem_ld(dsmem_addr(&ctrl.wmax, rk));
+            }
+            cnt = min(cnt, wcap);
+            const uint32_t incl = warp_incl_scan(cnt);
+            ctrl.warp_ties[lane] = incl - cnt;   // offset of the group's CTA `lane`
+            ctrl.warp_zeros[lane] = cnt;
+            mn = __reduce_min_sync(kFull, mn);
+            mx = __reduce_max_sync(kFull, mx);
+            if (lane == 31) ctrl.sel[0] = incl;
+            if (lane == 0) {
+                ctrl.sel[1] = mn;
+                ctrl.sel[2] = mx;
+            }
         }
         __syncthreads();
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const uint32_t x = b + (uint32_t)i * THREADS + tid;
-            if (x < n_peer) win[n_local + x] = t[i];
+        n = ctrl.sel[0];
+        for (uint32_t gr = 0; gr < gsize; ++gr) {
+            const uint32_t cnt = ctrl.warp_zeros[gr], off = ctrl.warp_ties[gr];
+            if (off + cnt > wcap) continue;   // flagged below
+            if (gr == 0) {
+                for (uint32_t i = tid; i < cnt; i += THREADS) cand[off + i] = win[i];
+            } else {
+                const uint32_t src = dsmem_addr(win, g0 + gr);
+                for (uint32_t i = tid; i < cnt; i += THREADS) cand[off + i] = dsmem_ld64(src + 8u * i);
+            }
         }
         __syncthreads();
     }
-    const uint32_t n_out = mode == kRange ? k_eff : n_gt;
-    if (n > 0) {
-        sort_and_write<THREADS>(win, reinterpret_cast<uint64_t *>(keys), (int)n, (int)min(n, n_out), (int)wcap,
-                                ctrl.wmin, ctrl.wmax, hist0, ctrl.scan64, oi, ov, idx_offset);
+    cluster_arrive();   // B4: the leaders have read every list
+    if (leader) {
+        const uint32_t expect = mode == kRange ? n_cand : n_gt;
+        if (n != expect || n > wcap) {
+            if (tid == 0) atomicOr(&g_status, TOPK_DEV_INTERNAL);
+            n = min(min(n, expect), wcap);
+        }
+        const uint32_t n_out = mode == kRange ? k_eff : n_gt;
+        if (n > 0) {
+            sort_and_write<THREADS>(cand, win, (int)n, (int)min(n, n_out), (int)wcap, ctrl.sel[1], ctrl.sel[2], hist0,
+                                    ctrl.scan64, oi, ov, idx_offset);
+        }
+        pad_out(oi, ov, (int)k_eff, p.k);
     }
-    pad_out(oi, ov, (int)k_eff, p.k);
+    cluster_wait();
 }
 
 // ------------------------------------------------------------------------- //
