@@ -60,6 +60,23 @@ def dist_env():
     return rank, world, local
 
 
+def max_over_ranks(ms: float, world: int) -> float:
+    """The slowest rank's time: the job's steps end when every rank's do."""
+    if world <= 1:
+        return ms
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([ms], dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, ms_per_step: float, world: int) -> float:
+    """Units per second over all ranks (weak scaling: each rank runs the
+    same workload on its own GPU, with no exchange between ranks)."""
+    return world * units_per_rank / (ms_per_step / 1e3)
+
+
 def algorithmic_bytes(total_len: int, B: int, k: int) -> int:
     """One read of every score, the index writes and the row metadata."""
     return 4 * total_len + 4 * B * k + 8 * B
@@ -328,13 +345,9 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize(device)
         if world > 1:
             torch.distributed.barrier()
-    ms = ev0.elapsed_time(ev1)
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world)
     ms_per_step = ms / args.steps
-    value = world * B / (ms_per_step / 1e3)
+    value = whole_job_rate(B, ms_per_step, world)
 
     # End to end through the public API with host buffers: pinned H2D of the
     # step's scores and metadata, the call, D2H of the indices.
@@ -365,7 +378,7 @@ def run_ours(args, rank, world, local):
             e2e_step()
         e1.record(stream)
         e1.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.e2e_steps
     e2e_parity = bool(np.array_equal(h_out.numpy(), ref))
 
     if rank != 0:
@@ -389,14 +402,14 @@ def run_ours(args, rank, world, local):
                          f" > 3x L2 {l2 / 1e6:.0f} MB): cold scores every step",
                    "timing": "CUDA events around graph replays of K launches on one stream",
                    "launch": info, "parity_vs_oracle": parity},
-        "elements_per_s": world * total / (ms_per_step / 1e3),
+        "elements_per_s": whole_job_rate(total, ms_per_step, world),
         "achieved_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
                      "traffic": stored_traffic(w.name),
                      "algorithmic_bytes_per_launch": alg},
         "cpu_baseline": cpu,
-        "e2e": {"value": world * B / (e2e_ms / 1e3), "unit": "rows/s",
+        "e2e": {"value": whole_job_rate(B, e2e_ms, world), "unit": "rows/s",
                 "h2d_bytes_per_step": h_scores.numel() * 4 + 8 * B,
                 "d2h_bytes_per_step": B * k * 4, "ms_per_step": e2e_ms,
                 "parity_vs_oracle": e2e_parity},
