@@ -284,7 +284,7 @@ def run_ours(args, rank, world, local):
     copies = [w.scores.clone() for _ in range(n_copies)]
     outs = [torch.empty((B, k), dtype=torch.int32, device=device) for _ in range(n_copies)]
     stream = torch.cuda.Stream(device)
-    info = pkg.launch_info(B, k, device)
+    info = pkg.launch_info(w.scores.numel(), B, k, device)
 
     def launch(i, s=stream):
         pkg.topk_ragged(copies[i], w.row_starts, w.lengths, k, w.offset_mode,

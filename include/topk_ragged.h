@@ -32,7 +32,7 @@
 extern "C" {
 #endif
 
-#define TOPK_RAGGED_ABI_VERSION 1
+#define TOPK_RAGGED_ABI_VERSION 2
 #define TOPK_RAGGED_MAX_K 4096
 /* Row lengths must stay below 2^24, the envelope of the 24-bit index field. */
 #define TOPK_RAGGED_MAX_LEN (1 << 24)
@@ -129,10 +129,11 @@ typedef struct {
 } topk_launch_info;
 
 /*
- * Fills *info for a call with (B, k) on the current device without launching
- * anything.  Returns TOPK_OK, TOPK_ERR_INVALID_ARG or the init error.
+ * Fills *info for a call with (n_scores, B, k) on the current device without
+ * launching anything.  Returns TOPK_OK, TOPK_ERR_INVALID_ARG or the init
+ * error.
  */
-int topk_ragged_launch_info(int32_t B, int32_t k, topk_launch_info *info);
+int topk_ragged_launch_info(int64_t n_scores, int32_t B, int32_t k, topk_launch_info *info);
 
 #ifdef __cplusplus
 }

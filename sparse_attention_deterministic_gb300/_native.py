@@ -92,7 +92,7 @@ def lib() -> ctypes.CDLL:
         so.topk_ragged.restype = ctypes.c_int
         so.topk_ragged_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_void_p]
         so.topk_ragged_device_status.restype = ctypes.c_int
-        so.topk_ragged_launch_info.argtypes = [ctypes.c_int32, ctypes.c_int32,
+        so.topk_ragged_launch_info.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                                ctypes.POINTER(LaunchInfo)]
         so.topk_ragged_launch_info.restype = ctypes.c_int
         _lib = so

@@ -106,13 +106,14 @@ def device_status(device=None, stream=None) -> int:
     return int(v.value)
 
 
-def launch_info(B: int, k: int, device=None) -> dict:
-    """How (B, k) is launched on the device: threads, cluster, grid, ..."""
+def launch_info(n_scores: int, B: int, k: int, device=None) -> dict:
+    """How a call with (n_scores, B, k) is launched on the device: threads,
+    cluster, grid, ..."""
     dev = torch.device("cuda", torch.cuda.current_device() if device is None else
                        torch.device(device).index or 0)
     info = LaunchInfo()
     with torch.cuda.device(dev):
-        rc = lib().topk_ragged_launch_info(int(B), int(k), ctypes.byref(info))
+        rc = lib().topk_ragged_launch_info(int(n_scores), int(B), int(k), ctypes.byref(info))
     if rc != 0:
         raise TopkError(rc, "topk_ragged_launch_info")
     return {name: int(getattr(info, name)) for name, _ in LaunchInfo._fields_}

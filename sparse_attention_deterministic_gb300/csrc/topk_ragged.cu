@@ -532,6 +532,7 @@ __device__ __forceinline__ void pad_out(int32_t *oi, float *ov, int from, int to
 // returns false with shared memory released and the general path runs.
 // ------------------------------------------------------------------------- //
 constexpr int kShortQuads = 4;
+constexpr int kShortScores = 4 * kShortQuads * 256;   // scores the one-CTA short path holds
 constexpr int kShortBucketBits = 12;   // 2 * kBins buckets with 16-bit counters
 
 template <int THREADS>
@@ -2099,7 +2100,7 @@ int stage_cap_for(int smem_budget, int off_keys)
     return ((smem_budget - off_keys) / 4) & ~127;
 }
 
-Plan make_plan(int32_t B, int32_t k, const DeviceInfo &dev)
+Plan make_plan(int64_t n_scores, int32_t B, int32_t k, const DeviceInfo &dev)
 {
     Plan pl{};
     const int sms = dev.sm_count;
@@ -2107,7 +2108,11 @@ Plan make_plan(int32_t B, int32_t k, const DeviceInfo &dev)
     // whatever the winner array's size (k <= 2 gives a single 8-byte slot).
     const int off_keys_cluster = (header_bytes(true) + list_cap(true, k) * 8 + 127) & ~127;
     int vi = 0, cluster = 1, smem_budget = 0, grid = B;
-    if (B < 4 * sms) {
+    // Short rows on average (the buffer holds at most kShortScores scores per
+    // row) go to the one-CTA-per-row kernel, whose short path ranks such a
+    // row in registers; clusters pay off for longer rows.
+    const bool short_rows = n_scores <= (int64_t)B * kShortScores;
+    if (B < 4 * sms && !short_rows) {
         double best = 0.0;
         for (int v = 2; v >= 1; --v) {
             const int budget = v == 2 ? dev.max_smem : dev.smem_per_sm / 2 - 1024;
@@ -2259,14 +2264,14 @@ static int validate(const float *scores, int64_t n_scores, const int32_t *row_st
     return TOPK_OK;
 }
 
-int topk_ragged_launch_info(int32_t B, int32_t k, topk_launch_info *info)
+int topk_ragged_launch_info(int64_t n_scores, int32_t B, int32_t k, topk_launch_info *info)
 {
-    if (!info || k < 1 || k > TOPK_RAGGED_MAX_K || B < 0) return TOPK_ERR_INVALID_ARG;
+    if (!info || k < 1 || k > TOPK_RAGGED_MAX_K || B < 0 || n_scores < 0) return TOPK_ERR_INVALID_ARG;
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess) return TOPK_ERR_CUDA;
     int rc = ensure_init(device, true);
     if (rc != TOPK_OK) return rc;
-    const Plan pl = make_plan(B, k, g_devices[device]);
+    const Plan pl = make_plan(n_scores, B, k, g_devices[device]);
     info->threads = pl.v->threads;
     info->cluster = pl.cluster;
     info->stage_cap = pl.stage_cap;
@@ -2289,7 +2294,7 @@ int topk_ragged(const float *scores, int64_t n_scores, const int32_t *row_starts
     if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return TOPK_ERR_CUDA;
     rc = ensure_init(device, cap == cudaStreamCaptureStatusNone);
     if (rc != TOPK_OK) return rc;
-    const Plan pl = make_plan(B, k, g_devices[device]);
+    const Plan pl = make_plan(n_scores, B, k, g_devices[device]);
 
     Params prm;
     prm.scores = scores;

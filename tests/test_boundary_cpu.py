@@ -39,7 +39,7 @@ def test_exports_every_declared_symbol(so):
 
 
 def test_abi_version_and_strerror(so):
-    assert so.topk_ragged_abi_version() == 1
+    assert so.topk_ragged_abi_version() == 2
     for st in range(5):
         assert pkg.strerror(st)
     assert pkg.strerror(99) == "unknown status"
@@ -68,7 +68,7 @@ def test_device_status_null(so):
 
 
 def test_launch_info_null(so):
-    assert so.topk_ragged_launch_info(4, 2048, None) == 1
+    assert so.topk_ragged_launch_info(16384, 4, 2048, None) == 1
 
 
 def test_header_defines_match_binding():

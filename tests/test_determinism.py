@@ -84,12 +84,18 @@ def test_batch_composition_invariance():
 
 
 def test_launch_shapes_cover_all_variants():
-    shapes = {B: pkg.launch_info(B, 2048) for B in (1, 4, 64, 300, 400, 4096)}
+    # Rows of 64k scores on average: clusters below four rows per SM.
+    shapes = {B: pkg.launch_info(B << 16, B, 2048) for B in (1, 4, 64, 300, 400, 4096)}
     kinds = {(info["threads"], info["cluster"] > 1) for info in shapes.values()}
     # 1024-thread clusters, 512-thread clusters (two CTAs per SM) and one
     # 256-thread CTA per row are all reached by some batch size.
     assert {(1024, True), (512, True), (256, False)} <= kinds, shapes
     assert shapes[4]["cluster"] == 16
+    # Batches of short rows (at most 4096 scores per row on average) take the
+    # one-CTA-per-row kernel whatever their size.
+    for B in (1, 4, 64):
+        info = pkg.launch_info(B * 4096, B, 2048)
+        assert info["cluster"] == 1 and info["grid"] == B
     assert shapes[4096]["cluster"] == 1 and shapes[4096]["grid"] == 4096
     for info in shapes.values():
         assert info["launches"] == 1
