@@ -1601,6 +1601,73 @@ __device__ void compact_slice(CCtrl &ctrl, const Slice &s, const uint32_t *keys,
     auto is_cand = [&](uint32_t e) { return EXACT ? e > T : e >= lo; };
     auto is_tie = [&](uint32_t e) { return EXACT && e == T; };
 
+    if constexpr (!EXACT) {
+        // Without ties the list's order is free: one pass, each warp round
+        // taking its slots with one atomic on the list length.
+        if (tid == 0) ctrl.win_local = 0u;
+        __syncthreads();
+        uint32_t wmin = kFull, wmax = 0;
+        auto put = [&](uint32_t e, int32_t j, uint32_t slot) {
+            wmin = min(wmin, e);
+            wmax = max(wmax, e);
+            if (slot < wcap) win[slot] = ((uint64_t)e << 32) | (uint64_t)(~(uint32_t)j);
+        };
+        if (pt.head >= 0 || pt.tail >= 0) {   // warp-uniform
+            for (int h = 0; h < 2; ++h) {
+                const int q = h == 0 ? pt.head : pt.tail;
+                if (q < 0) continue;
+                uint32_t c = 0, m = 0;
+                uint4 kk = make_uint4(0, 0, 0, 0);
+                if (lane == 0) {
+                    kk = partial_quad(s, keys4, q, m);
+                    const uint32_t e[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i) c += ((m >> i) & 1u) && e[i] >= lo;
+                }
+                uint32_t base = 0;
+                if (lane == 0 && c) base = atomicAdd(&ctrl.win_local, c);
+                if (lane == 0 && c) {
+                    const uint32_t e[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+                    for (int i = 0; i < 4; ++i)
+                        if (((m >> i) & 1u) && e[i] >= lo) put(e[i], s.jbase + 4 * q + i, base++);
+                }
+            }
+        }
+        body_rounds<U, STAGED>(s, keys4, pt, [&](int qb, const uint4 (&kk)[U], const bool (&ok)[U]) {
+            uint32_t cm = 0;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                if (!(ok[u] && quad_max(kk[u]) >= lo)) continue;
+                const uint32_t e[4] = {kk[u].x, kk[u].y, kk[u].z, kk[u].w};
+#pragma unroll
+                for (int i = 0; i < 4; ++i) cm |= (uint32_t)(e[i] >= lo) << (4 * u + i);
+            }
+            if (!__any_sync(kFull, cm != 0)) return;
+            const uint32_t cnt = (uint32_t)__popc(cm);
+            const uint32_t ci = warp_incl_scan(cnt);
+            uint32_t base = 0;
+            if (lane == 31) base = atomicAdd(&ctrl.win_local, ci);
+            uint32_t slot = __shfl_sync(kFull, base, 31) + ci - cnt;
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const uint32_t e[4] = {kk[u].x, kk[u].y, kk[u].z, kk[u].w};
+                const int32_t j0 = s.jbase + 4 * (qb + u * 32 + lane);
+#pragma unroll
+                for (int i = 0; i < 4; ++i)
+                    if ((cm >> (4 * u + i)) & 1u) put(e[i], j0 + i, slot++);
+            }
+        });
+        wmin = __reduce_min_sync(kFull, wmin);
+        wmax = __reduce_max_sync(kFull, wmax);
+        if (lane == 0 && wmin != kFull) {
+            atomicMin(&ctrl.wmin, wmin);
+            atomicMax(&ctrl.wmax, wmax);
+        }
+        __syncthreads();
+        return;
+    }
+
     // Count pass.
     uint32_t nc = 0, nt = 0;
     auto count = [&](uint32_t e, bool v) {
