@@ -29,6 +29,9 @@ _lib = None
 
 FLAG_LEN_ENVELOPE = 1
 FLAG_BAD_WINDOW = 2
+# offset_mode bits
+OFFSET_ROW_START = 1
+EXCLUDE_NEG_INF = 2   # leave out -inf and every negative NaN
 PAD_VALUE_BITS = 0xFF800000
 
 

@@ -36,6 +36,14 @@
  *               flagged (bit 1).  A window not inside [0, n_scores) is written
  *               as all -1 and flagged (bit 2): the flat-buffer reading of the
  *               same commit's clamping of windows against trusted metadata.
+ *   exclusion   with offset_mode bit 2 set, the scores at or below -inf in the
+ *               total order (-inf and every negative NaN) are left out
+ *               before the selection: the row holds the first min(k, m) of
+ *               the m remaining entries, then -1.  This reads the sglang
+ *               page's torch-compatible backend (Modifications), which
+ *               leaves -inf scores out; the negative NaNs, which rank below
+ *               -inf, go with them, so the excluded entries are exactly a
+ *               tail of the order.
  *
  * Method: per row, build (order key, index) pairs and sort them with qsort
  * under an explicit comparator.  No blocking, no radix, no fusion.
@@ -49,6 +57,9 @@
 #define ORACLE_MAX_LEN ((int64_t)1 << 24)
 #define ORACLE_FLAG_LEN_ENVELOPE 1u
 #define ORACLE_FLAG_BAD_WINDOW 2u
+/* offset_mode bits: indices offset by the row start; -inf excluded. */
+#define ORACLE_OFFSET_ROW_START 1
+#define ORACLE_EXCLUDE_NEG_INF 2
 
 /* Order key of one fp32 bit pattern.  For a non-negative float (sign bit
  * clear) setting the sign bit moves it above every negative pattern while
@@ -141,18 +152,27 @@ static void *oracle_worker(void *arg)
                 return NULL;
             }
         }
+        /* With the exclusion flag the scores at or below -inf in the total
+         * order (-inf and every negative NaN) are not candidates at all. */
+        const int exclude = (job->offset_mode & ORACLE_EXCLUDE_NEG_INF) != 0;
+        const uint32_t neg_inf_key = oracle_order_key(0xFF800000u);
+        int64_t m = 0;
         for (int64_t j = 0; j < len; ++j) {
             uint32_t bits;
             memcpy(&bits, &job->scores[start + j], 4);
-            pairs[j].key = oracle_order_key(bits);
-            pairs[j].idx = (int32_t)j;
+            const uint32_t key = oracle_order_key(bits);
+            if (exclude && key <= neg_inf_key)
+                continue;
+            pairs[m].key = key;
+            pairs[m].idx = (int32_t)j;
+            ++m;
         }
-        qsort(pairs, (size_t)len, sizeof(oracle_pair), oracle_cmp);
-        int32_t n = len < job->k ? (int32_t)len : job->k;
+        qsort(pairs, (size_t)m, sizeof(oracle_pair), oracle_cmp);
+        int32_t n = m < job->k ? (int32_t)m : job->k;
         for (int32_t p = 0; p < n; ++p) {
             int32_t j = pairs[p].idx;
             job->out_idx[row * job->k + p] =
-                job->offset_mode == 1 ? (int32_t)(start + j) : j;
+                (job->offset_mode & ORACLE_OFFSET_ROW_START) ? (int32_t)(start + j) : j;
             if (job->out_val)
                 job->out_val[row * job->k + p] = job->scores[start + j];
         }
@@ -163,7 +183,8 @@ static void *oracle_worker(void *arg)
 }
 
 /* Returns 0 on success, -1 on an argument the selection does not define
- * (k outside [1, 4096], B < 0, offset_mode outside {0, 1}, a null buffer),
+ * (k outside [1, 4096], B < 0, offset_mode other than a combination of
+ * ORACLE_OFFSET_ROW_START and ORACLE_EXCLUDE_NEG_INF, a null buffer),
  * -2 if a worker could not allocate its pair buffer.  row_flags (nullable)
  * receives the per-row envelope/window flags described above. */
 int oracle_topk_ragged(const float *scores, int64_t n_scores,
@@ -172,7 +193,7 @@ int oracle_topk_ragged(const float *scores, int64_t n_scores,
                        int32_t *out_idx, float *out_val, uint32_t *row_flags,
                        int n_threads)
 {
-    if (k < 1 || k > ORACLE_MAX_K || B < 0 || (offset_mode != 0 && offset_mode != 1))
+    if (k < 1 || k > ORACLE_MAX_K || B < 0 || (offset_mode & ~3) != 0)
         return -1;
     if (B == 0)
         return 0;

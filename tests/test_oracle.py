@@ -296,7 +296,7 @@ def test_empty_batch_and_bad_args():
         with pytest.raises(ValueError):
             oracle.topk_ragged(flat, np.array([0]), np.array([4]), k)
     with pytest.raises(ValueError):
-        oracle.topk_ragged(flat, np.array([0]), np.array([4]), 2, offset_mode=2)
+        oracle.topk_ragged(flat, np.array([0]), np.array([4]), 2, offset_mode=4)
 
 
 @pytest.mark.parametrize("T", [64, 512, 4096])
@@ -339,6 +339,63 @@ def test_offset_mode_shift():
     glob_, v1, _ = oracle.topk_ragged(s, st, ln, 512, 1)
     np.testing.assert_array_equal(glob_, np.where(local >= 0, local + st[:, None], -1))
     np.testing.assert_array_equal(v0.view(np.uint32), v1.view(np.uint32))
+
+
+# --------------------------------------------------------------------------- #
+# The -inf exclusion flag (offset_mode bit 2): -inf and every negative NaN
+# are left out of the selection (the sglang page's torch-compatible backend,
+# Modifications, leaves -inf scores out; the negative NaNs rank below -inf
+# and go with them).
+# --------------------------------------------------------------------------- #
+
+def _bits(values):
+    return np.array(values, dtype=np.uint32).view(np.float32)
+
+
+def test_exclusion_closed_form():
+    # [3, -inf, 1, -NaN, 2, -inf]: the three finite scores in value order,
+    # then -1; values -inf in the padding.
+    row = _bits([0x40400000, 0xFF800000, 0x3F800000, 0xFFC00000, 0x40000000, 0xFF800000])
+    idx, val, _ = oracle.topk_ragged(row, np.array([0], np.int32), np.array([6], np.int32), 6,
+                                     oracle.EXCLUDE_NEG_INF)
+    assert list(idx[0]) == [0, 4, 2, -1, -1, -1]
+    assert list(val[0].view(np.uint32)) == [0x40400000, 0x40000000, 0x3F800000] + [0xFF800000] * 3
+    # Without the flag -inf ranks by its key above the negative NaN.
+    idx, _, _ = oracle.topk_ragged(row, np.array([0], np.int32), np.array([6], np.int32), 6, 0)
+    assert list(idx[0]) == [0, 4, 2, 1, 5, 3]
+
+
+def test_exclusion_all_neg_inf_row():
+    row = np.full(100, -np.inf, dtype=np.float32)
+    idx, val, _ = oracle.topk_ragged(row, np.array([0], np.int32), np.array([100], np.int32), 64,
+                                     oracle.EXCLUDE_NEG_INF | oracle.OFFSET_ROW_START)
+    assert (idx == -1).all()
+    assert (val.view(np.uint32) == 0xFF800000).all()
+
+
+@pytest.mark.parametrize("mode", [oracle.EXCLUDE_NEG_INF, oracle.EXCLUDE_NEG_INF | oracle.OFFSET_ROW_START])
+def test_exclusion_equals_selection_of_the_kept_entries(mode):
+    """Flag on == the plain selection of the row with the excluded entries
+    removed, indices mapped back: a second route to the same result."""
+    rng = np.random.default_rng(29)
+    alphabet = np.array([0xFF800000, 0xFFC00000, 0xFFC00123, 0x7FC00000, 0x80000000, 0,
+                         0x3F800000, 0xBF800000, 0x7F800000, 0x40000000], dtype=np.uint32)
+    for _ in range(300):
+        L = int(rng.integers(0, 40))
+        k = int(rng.integers(1, 48))
+        start = int(rng.integers(0, 5))
+        bits = rng.choice(alphabet, size=L)
+        flat = np.concatenate([np.zeros(start, np.uint32), bits]).view(np.float32)
+        got, _, _ = oracle.topk_ragged(flat, np.array([start], np.int32), np.array([L], np.int32), k, mode)
+        keys = oracle.order_key(bits).astype(np.int64)
+        neg_inf_key = int(oracle.order_key(np.array([0xFF800000], np.uint32))[0])
+        keep = np.nonzero(keys > neg_inf_key)[0]
+        sub = bits[keep].view(np.float32)
+        ref, _, _ = oracle.topk_ragged(sub, np.array([0], np.int32), np.array([keep.size], np.int32), k, 0)
+        ref = np.where(ref[0] >= 0, keep[np.maximum(ref[0], 0)], -1) if keep.size else ref[0]
+        if mode & oracle.OFFSET_ROW_START:
+            ref = np.where(ref >= 0, ref + start, -1)
+        assert list(got[0]) == list(ref)
 
 
 # --------------------------------------------------------------------------- #

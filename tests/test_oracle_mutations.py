@@ -22,9 +22,10 @@ MUTATIONS = {
     "negative_branch_sign_flip": ("return ~bits;", "return bits ^ 0x80000000u;"),
     "positive_branch_no_or": ("return bits | 0x80000000u;", "return bits;"),
     "pad_value_zero": ("neg_inf_bits = 0xFF800000u", "neg_inf_bits = 0x00000000u"),
-    "offset_ignored": ("job->offset_mode == 1 ? (int32_t)(start + j) : j", "j"),
-    "one_short": ("int32_t n = len < job->k ? (int32_t)len : job->k;",
-                  "int32_t n = len < job->k ? (int32_t)len : job->k - 1;"),
+    "offset_ignored": ("(job->offset_mode & ORACLE_OFFSET_ROW_START) ? (int32_t)(start + j) : j", "j"),
+    "exclusion_ignored": ("if (exclude && key <= neg_inf_key)", "if (0)"),
+    "one_short": ("int32_t n = m < job->k ? (int32_t)m : job->k;",
+                  "int32_t n = m < job->k ? (int32_t)m : job->k - 1;"),
     "length_envelope_off": ("if (len >= ORACLE_MAX_LEN)", "if (len > ORACLE_MAX_LEN)"),
 }
 
@@ -85,6 +86,16 @@ def _pins_pass(so):
         for r, row in enumerate(rows):
             if list(idx[r]) != brute_force_topk([int(b) for b in row], k):
                 return False
+    # Exclusion of -inf and negative NaN (offset_mode bit 2), with and
+    # without the row-start offset: [3, -inf, 1, -NaN, 2, -inf], k = 6.
+    row = np.array([0x40400000, 0xFF800000, 0x3F800000, 0xFFC00000, 0x40000000, 0xFF800000],
+                   dtype=np.uint32)
+    flat = np.concatenate([np.zeros(5, np.uint32), row])
+    for mode, want in ((2, [0, 4, 2, -1, -1, -1]), (3, [5, 9, 7, -1, -1, -1]),
+                       (0, [0, 4, 2, 1, 5, 3])):
+        idx, _, _ = _call(so, flat, [5], [6], 6, mode)
+        if list(idx[0]) != want:
+            return False
     ones = np.ones(64, dtype=np.float32).view(np.uint32)
     _, _, flags = _call(so, ones, [0, 0], [1 << 24, 4], 2, 0)
     if list(flags) != [oracle.FLAG_LEN_ENVELOPE, 0]:
