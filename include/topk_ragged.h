@@ -46,10 +46,17 @@ typedef enum {
     TOPK_ERR_CUDA = 4                /* a CUDA runtime call or launch failed    */
 } topk_status;
 
-/* offset_mode values. */
+/* offset_mode: TOPK_OFFSET_ROW_LOCAL or TOPK_OFFSET_ROW_START, optionally
+ * or-ed with TOPK_EXCLUDE_NEG_INF. */
 enum {
     TOPK_OFFSET_ROW_LOCAL = 0, /* out_idx holds j, the index inside the row      */
-    TOPK_OFFSET_ROW_START = 1  /* out_idx holds row_starts[i] + j (buffer index) */
+    TOPK_OFFSET_ROW_START = 1, /* out_idx holds row_starts[i] + j (buffer index) */
+    /* Leave out -inf and every negative NaN (the scores at or below -inf in
+     * the order): the row holds the selection of its other entries, front-
+     * packed, then -1.  The torch-compatible backend of sglang PR #31115
+     * (Modifications) leaves -inf scores out; without this bit -inf ranks by
+     * its key like any score. */
+    TOPK_EXCLUDE_NEG_INF = 2
 };
 
 /* Bits of the device status word (data errors found by the kernel). */
@@ -91,7 +98,8 @@ int topk_ragged_init(int device);
  *              Windows may overlap, be unaligned and come in any order.
  * B            number of rows, B >= 0; B == 0 returns TOPK_OK with no launch.
  * k            1 <= k <= 4096, and (int64)B * k < 2^31.
- * offset_mode  TOPK_OFFSET_ROW_LOCAL or TOPK_OFFSET_ROW_START.
+ * offset_mode  TOPK_OFFSET_ROW_LOCAL or TOPK_OFFSET_ROW_START, optionally
+ *              or-ed with TOPK_EXCLUDE_NEG_INF.
  * out_idx      device, int32[B, k] row-major, written entirely: row i holds
  *              the min(k, L_i) selected indices in canonical order, then -1.
  * out_val      device, fp32[B, k] or NULL: the selected scores' original bit

@@ -10,11 +10,13 @@ loads and calls it.
 from ._native import EXPORTS, LIB_PATH, TopkError, build, lib, strerror
 from .binding import (MAX_K, MAX_LEN, PAD_VALUE_BITS, TOPK_DEV_BAD_WINDOW,
                       TOPK_DEV_INTERNAL, TOPK_DEV_LEN_ENVELOPE, TOPK_OFFSET_ROW_LOCAL,
-                      TOPK_OFFSET_ROW_START, device_status, init, launch_info, topk_ragged)
+                      TOPK_EXCLUDE_NEG_INF, TOPK_OFFSET_ROW_START, device_status, init, launch_info,
+                      topk_ragged)
 
 __all__ = [
     "EXPORTS", "LIB_PATH", "TopkError", "build", "lib", "strerror", "MAX_K", "MAX_LEN",
     "PAD_VALUE_BITS", "TOPK_DEV_BAD_WINDOW", "TOPK_DEV_INTERNAL", "TOPK_DEV_LEN_ENVELOPE",
-    "TOPK_OFFSET_ROW_LOCAL", "TOPK_OFFSET_ROW_START", "device_status", "init", "launch_info",
+    "TOPK_OFFSET_ROW_LOCAL", "TOPK_OFFSET_ROW_START", "TOPK_EXCLUDE_NEG_INF", "device_status", "init",
+    "launch_info",
     "topk_ragged",
 ]

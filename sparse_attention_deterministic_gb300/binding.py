@@ -16,6 +16,7 @@ from ._native import LaunchInfo, TopkError, lib
 
 TOPK_OFFSET_ROW_LOCAL = 0
 TOPK_OFFSET_ROW_START = 1
+TOPK_EXCLUDE_NEG_INF = 2   # or-ed into offset_mode: leave out -inf and negative NaN
 TOPK_DEV_LEN_ENVELOPE = 1
 TOPK_DEV_BAD_WINDOW = 2
 TOPK_DEV_INTERNAL = 4

@@ -98,6 +98,21 @@ __device__ __forceinline__ uint32_t key_bits(uint32_t key)
     return (key & 0x80000000u) ? (key & 0x7FFFFFFFu) : ~key;
 }
 
+constexpr uint32_t kNegInfKey = 0x007FFFFFu;   // order key of -inf
+
+// Writes one selected entry at output place pos: its index (plus the row
+// offset) and its score, or -1 / -inf when the exclusion flag leaves the
+// score out.  Excluded scores (-inf and every negative NaN: keys at or
+// below that of -inf) rank after all others, so they fill a tail of the
+// selection and the row stays front-packed.
+__device__ __forceinline__ void put_out(int32_t *oi, float *ov, uint32_t pos, int64_t idx_offset, int32_t j,
+                                        uint32_t key, bool excl)
+{
+    const bool drop = excl && key <= kNegInfKey;
+    oi[pos] = drop ? -1 : (int32_t)(idx_offset + j);
+    if (ov) ov[pos] = __uint_as_float(drop ? kNegInfBits : key_bits(key));
+}
+
 // ------------------------------------------------------------------------- //
 // Cluster / DSMEM primitives (inline PTX).
 // ------------------------------------------------------------------------- //
@@ -442,7 +457,7 @@ __device__ __forceinline__ uint64_t block_incl_scan64(uint64_t x, uint64_t *sm, 
 template <int THREADS>
 __device__ void sort_and_write(uint64_t *a, uint64_t *b, int n, int n_out, int cap_pow2, uint32_t kmin,
                                uint32_t kmax, uint32_t *cur, uint64_t *sm64, int32_t *oi, float *ov,
-                               int64_t idx_offset)
+                               int64_t idx_offset, bool excl)
 {
     constexpr int BPT = kBins / THREADS;
     const int tid = threadIdx.x;
@@ -471,8 +486,7 @@ __device__ void sort_and_write(uint64_t *a, uint64_t *b, int n, int n_out, int c
         bitonic_desc<THREADS>(a, (uint32_t)n2);
         for (int p = tid; p < n_out; p += THREADS) {
             const uint64_t c = a[p];
-            oi[p] = (int32_t)(idx_offset + (int32_t)(~(uint32_t)c));
-            if (ov) ov[p] = __uint_as_float(key_bits((uint32_t)(c >> 32)));
+            put_out(oi, ov, (uint32_t)p, idx_offset, (int32_t)(~(uint32_t)c), (uint32_t)(c >> 32), excl);
         }
         return;
     }
@@ -498,10 +512,8 @@ __device__ void sort_and_write(uint64_t *a, uint64_t *b, int n, int n_out, int c
         uint32_t rank = 0;
         for (uint32_t q = st; q < en; ++q) rank += b[q] > x;
         const uint32_t pos = st + rank;
-        if (pos < (uint32_t)n_out) {
-            oi[pos] = (int32_t)(idx_offset + (int32_t)(~(uint32_t)x));
-            if (ov) ov[pos] = __uint_as_float(key_bits((uint32_t)(x >> 32)));
-        }
+        if (pos < (uint32_t)n_out)
+            put_out(oi, ov, pos, idx_offset, (int32_t)(~(uint32_t)x), (uint32_t)(x >> 32), excl);
     }
 }
 
@@ -537,7 +549,7 @@ constexpr int kShortBucketBits = 12;   // 2 * kBins buckets with 16-bit counters
 
 template <int THREADS>
 __device__ bool short_row(Ctrl &ctrl, uint32_t *cur, uint64_t *buf, uint32_t buf_cap, const Slice &s,
-                          uint32_t k_eff, int64_t idx_offset, int32_t *oi, float *ov, int k)
+                          uint32_t k_eff, int64_t idx_offset, int32_t *oi, float *ov, int k, bool excl)
 {
     constexpr int NW = THREADS / 32;
     constexpr int BPT = kBins / THREADS;
@@ -729,10 +741,7 @@ __device__ bool short_row(Ctrl &ctrl, uint32_t *cur, uint64_t *buf, uint32_t buf
 #pragma unroll 1
             for (uint32_t y = st; y < en; ++y) pos += buf[y] > c;
             if (e < kZ) pos += Zc;
-            if (pos < k_eff) {
-                oi[pos] = (int32_t)(idx_offset + (int32_t)(~(uint32_t)c));
-                if (ov) ov[pos] = __uint_as_float(key_bits(e));
-            }
+            if (pos < k_eff) put_out(oi, ov, pos, idx_offset, (int32_t)(~(uint32_t)c), e, excl);
         }
     }
     pad_out(oi, ov, (int)k_eff, k);
@@ -917,7 +926,8 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_row_kernel(c
     }
     const int32_t L = (int32_t)len;
     const uint32_t k_eff = (uint32_t)(p.k < L ? p.k : L);
-    const int64_t idx_offset = p.offset_mode == TOPK_OFFSET_ROW_START ? rs : 0;
+    const int64_t idx_offset = (p.offset_mode & TOPK_OFFSET_ROW_START) ? rs : 0;
+    const bool excl = (p.offset_mode & TOPK_EXCLUDE_NEG_INF) != 0;
 
     // ---- slice of this CTA (16-byte aligned body split by quads) ----------- //
     Slice s;
@@ -941,7 +951,7 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_row_kernel(c
     }
     if (s.nq <= kShortQuads * THREADS) {
         const uint32_t cap = (uint32_t)(p.off_keys + p.stage_cap * 4 - p.off_win) / 8u;
-        if (short_row<THREADS>(ctrl, hist, win, cap, s, k_eff, idx_offset, oi, ov, p.k)) return;
+        if (short_row<THREADS>(ctrl, hist, win, cap, s, k_eff, idx_offset, oi, ov, p.k, excl)) return;
     }
     const WarpSeg seg = warp_segment<THREADS>(s.nq, warp);
 
@@ -1076,7 +1086,6 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_row_kernel(c
         if (sel_done) break;
     }
     const uint32_t T = prefix;   // exact k-th key; n_gt above it, take r of its cnt ties
-    const uint32_t tval = key_bits(T);
 
     // ---- a6+a7: one pass over the slice.  Winners (key > T) go to the
     //      list in any order (their composites are unique, the sort makes
@@ -1166,8 +1175,7 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_row_kernel(c
                             if ((tm >> i) & 1u) {
                                 if (tord < r && n_gt + tord < k_eff) {
                                     const int32_t j = s.jbase + 4 * q + i;
-                                    oi[n_gt + tord] = (int32_t)(idx_offset + j);
-                                    if (ov) ov[n_gt + tord] = __uint_as_float(tval);
+                                    put_out(oi, ov, n_gt + tord, idx_offset, j, T, excl);
                                 }
                                 ++tord;
                             }
@@ -1221,8 +1229,7 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_row_kernel(c
                         if ((tm >> i) & 1u) {
                             if (tord < r && n_gt + tord < k_eff) {
                                 const int32_t j = s.jbase + 4 * q + i;
-                                oi[n_gt + tord] = (int32_t)(idx_offset + j);
-                                if (ov) ov[n_gt + tord] = __uint_as_float(tval);
+                                put_out(oi, ov, n_gt + tord, idx_offset, j, T, excl);
                             }
                             ++tord;
                         }
@@ -1242,7 +1249,7 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_row_kernel(c
     const uint32_t n_sort = n_gt < (uint32_t)p.win_cap ? n_gt : (uint32_t)p.win_cap;
     if (n_sort > 0) {
         sort_and_write<THREADS>(win, reinterpret_cast<uint64_t *>(keys), (int)n_sort, (int)n_sort, p.win_cap,
-                                ctrl.wmin, ctrl.kmax, hist, ctrl.scan64, oi, ov, idx_offset);
+                                ctrl.wmin, ctrl.kmax, hist, ctrl.scan64, oi, ov, idx_offset, excl);
     }
     pad_out(oi, ov, (int)k_eff, p.k);
 }
@@ -1592,7 +1599,7 @@ __device__ void level_pass(const Slice &s, const uint32_t *keys, const Parts &pt
 template <int THREADS, bool EXACT, bool STAGED>
 __device__ void compact_slice(CCtrl &ctrl, const Slice &s, const uint32_t *keys, const Parts &pt, uint64_t *win,
                               uint32_t wcap, uint32_t lo, uint32_t T, uint32_t tie_base, uint32_t r, uint32_t n_gt,
-                              uint32_t k_eff, int64_t idx_offset, int32_t *oi, float *ov)
+                              uint32_t k_eff, int64_t idx_offset, int32_t *oi, float *ov, bool excl)
 {
     constexpr int NW = THREADS / 32;
     constexpr int U = kPassQuads;
@@ -1728,10 +1735,7 @@ __device__ void compact_slice(CCtrl &ctrl, const Slice &s, const uint32_t *keys,
         if (slot < wcap) win[slot] = ((uint64_t)e << 32) | (uint64_t)(~(uint32_t)j);
     };
     auto put_tie = [&](int32_t j, uint32_t ord) {
-        if (ord < r && n_gt + ord < k_eff) {
-            oi[n_gt + ord] = (int32_t)(idx_offset + j);
-            if (ov) ov[n_gt + ord] = __uint_as_float(key_bits(T));
-        }
+        if (ord < r && n_gt + ord < k_eff) put_out(oi, ov, n_gt + ord, idx_offset, j, T, excl);
     };
     // A partial quad of this warp, written by lane 0 at the warp's cursors.
     auto partial = [&](int q) {
@@ -1833,14 +1837,14 @@ template <int THREADS, bool EXACT>
 __device__ __forceinline__ void compact(bool staged, CCtrl &ctrl, const Slice &s, const uint32_t *keys,
                                         const Parts &pt, const Parts &ptm, uint64_t *win, uint32_t wcap, uint32_t lo,
                                         uint32_t T, uint32_t tie_base, uint32_t r, uint32_t n_gt, uint32_t k_eff,
-                                        int64_t idx_offset, int32_t *oi, float *ov)
+                                        int64_t idx_offset, int32_t *oi, float *ov, bool excl)
 {
     if (staged && (EXACT ? T != 0u : lo != 0u))
         compact_slice<THREADS, EXACT, true>(ctrl, s, keys, pt, win, wcap, lo, T, tie_base, r, n_gt, k_eff, idx_offset,
-                                            oi, ov);
+                                            oi, ov, excl);
     else
         compact_slice<THREADS, EXACT, false>(ctrl, s, keys, ptm, win, wcap, lo, T, tie_base, r, n_gt, k_eff,
-                                             idx_offset, oi, ov);
+                                             idx_offset, oi, ov, excl);
 }
 
 template <int THREADS>
@@ -1869,7 +1873,8 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
     const int64_t rs = g.start;
     const int32_t L = g.len;
     const uint32_t k_eff = (uint32_t)(p.k < L ? p.k : L);
-    const int64_t idx_offset = p.offset_mode == TOPK_OFFSET_ROW_START ? rs : 0;
+    const int64_t idx_offset = (p.offset_mode & TOPK_OFFSET_ROW_START) ? rs : 0;
+    const bool excl = (p.offset_mode & TOPK_EXCLUDE_NEG_INF) != 0;
     int32_t *oi = p.out_idx + (int64_t)row * p.k;
     float *ov = p.out_val ? p.out_val + (int64_t)row * p.k : nullptr;
 
@@ -1987,10 +1992,10 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
     if (mode != kRefine) {
         if (plateau)
             compact<THREADS, true>(staged, ctrl, s, keys, pt, ptm, win, wcap, 0u, T, ties_before(&ctrl.zeros), r,
-                                   n_gt, k_eff, idx_offset, oi, ov);
+                                   n_gt, k_eff, idx_offset, oi, ov, excl);
         else
             compact<THREADS, false>(staged, ctrl, s, keys, pt, ptm, win, wcap, lo_key, 0u, 0u, r, n_gt, k_eff,
-                                    idx_offset, oi, ov);
+                                    idx_offset, oi, ov, excl);
     } else {
         refine_pass<THREADS>(staged, s, keys, pt, ptm, hist1, prefix, 21, 10, 0x7FFu);
         __syncthreads();
@@ -2005,7 +2010,7 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
             lo_key = (prefix << 21) | (d << 10);
             n_cand = n_gt + gt + c;
             compact<THREADS, false>(staged, ctrl, s, keys, pt, ptm, win, wcap, lo_key, 0u, 0u, r, n_gt, k_eff,
-                                    idx_offset, oi, ov);
+                                    idx_offset, oi, ov, excl);
             } else {
             prefix = (prefix << 11) | d;
             n_gt += gt;
@@ -2028,7 +2033,7 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
         r -= gt;
         const uint32_t tb = ties_before(&hist0[T & 0x3FFu]);
         compact<THREADS, true>(staged, ctrl, s, keys, pt, ptm, win, wcap, 0u, T, tb, r, n_gt, k_eff, idx_offset, oi,
-                               ov);
+                               ov, excl);
     }
     cluster_sync();   // B3: every CTA's candidate list is final
 
@@ -2082,7 +2087,7 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
         const uint32_t n_out = mode == kRange ? k_eff : n_gt;
         if (n > 0) {
             sort_and_write<THREADS>(cand, win, (int)n, (int)min(n, n_out), (int)wcap, ctrl.sel[1], ctrl.sel[2], hist0,
-                                    ctrl.scan64, oi, ov, idx_offset);
+                                    ctrl.scan64, oi, ov, idx_offset, excl);
         }
         pad_out(oi, ov, (int)k_eff, p.k);
     }
@@ -2321,8 +2326,7 @@ static int validate(const float *scores, int64_t n_scores, const int32_t *row_st
 {
     if (k < 1 || k > TOPK_RAGGED_MAX_K || B < 0) return TOPK_ERR_INVALID_ARG;
     if ((int64_t)B * (int64_t)k >= ((int64_t)1 << 31)) return TOPK_ERR_INVALID_ARG;
-    if (offset_mode != TOPK_OFFSET_ROW_LOCAL && offset_mode != TOPK_OFFSET_ROW_START)
-        return TOPK_ERR_INVALID_ARG;
+    if ((offset_mode & ~(TOPK_OFFSET_ROW_START | TOPK_EXCLUDE_NEG_INF)) != 0) return TOPK_ERR_INVALID_ARG;
     if (n_scores < 0 || n_scores >= ((int64_t)1 << 31)) return TOPK_ERR_INVALID_ARG;
     if (B == 0) return TOPK_OK;
     if (!row_starts || !lengths || !out_idx) return TOPK_ERR_INVALID_ARG;

@@ -50,7 +50,7 @@ def _call(so, scores=0x1000, n=16, rs=0x2000, ln=0x3000, B=1, k=4, mode=0, oi=0x
 
 
 @pytest.mark.parametrize("kw", [
-    dict(k=0), dict(k=4097), dict(k=-1), dict(B=-1), dict(mode=2), dict(mode=-1),
+    dict(k=0), dict(k=4097), dict(k=-1), dict(B=-1), dict(mode=4), dict(mode=-1),
     dict(rs=None), dict(ln=None), dict(oi=None), dict(scores=None),
     dict(scores=0x1002), dict(n=-1), dict(n=1 << 31), dict(B=1 << 20, k=4096),
 ])
