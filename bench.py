@@ -50,6 +50,9 @@ def parse_args():
     p.add_argument("--e2e-steps", type=int, default=500)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--page-size", type=int, default=0,
+                   help="write KV-cache slots through random per-row page tables of this "
+                        "page size (topk_ragged_paged); 0: plain indices")
     return p.parse_args()
 
 
@@ -286,9 +289,19 @@ def run_ours(args, rank, world, local):
     stream = torch.cuda.Stream(device)
     info = pkg.launch_info(w.scores.numel(), B, k, device)
 
+    # The page-table transform: random per-row page tables (the row-start
+    # offset has no meaning there, so the mode keeps only its other bits).
+    page_table, mode = None, w.offset_mode
+    if args.page_size > 0:
+        n_pages = -(-int(w.lengths.max()) // args.page_size)
+        g = torch.Generator().manual_seed(1234)
+        page_table = torch.stack([torch.randperm(4 * n_pages, generator=g)[:n_pages] for _ in range(B)]
+                                 ).to(torch.int32).to(device)
+        mode = w.offset_mode & ~pkg.TOPK_OFFSET_ROW_START
+
     def launch(i, s=stream):
-        pkg.topk_ragged(copies[i], w.row_starts, w.lengths, k, w.offset_mode,
-                        out_idx=outs[i], stream=s)
+        pkg.topk_ragged(copies[i], w.row_starts, w.lengths, k, mode, out_idx=outs[i], stream=s,
+                        page_table=page_table, page_size=max(args.page_size, 1))
 
     # Parity guard: the timed configuration must match the oracle on this input.
     import numpy as np
@@ -298,8 +311,10 @@ def run_ours(args, rank, world, local):
         launch(0)
     stream.synchronize()
     s_np, st_np, ln_np = w.numpy()
-    ref, _, _ = oracle.topk_ragged(s_np, st_np, ln_np, k, w.offset_mode,
+    ref, _, _ = oracle.topk_ragged(s_np, st_np, ln_np, k, mode,
                                    n_threads=len(os.sched_getaffinity(0)), with_values=False)
+    if page_table is not None:
+        ref = oracle.paged_slots(ref, page_table.cpu().numpy(), args.page_size)
     parity = bool(np.array_equal(outs[0].cpu().numpy(), ref))
     if pkg.device_status(device) != 0:
         parity = False
@@ -364,7 +379,8 @@ def run_ours(args, rank, world, local):
         d_scores.copy_(h_scores, non_blocking=True)
         d_starts.copy_(h_starts, non_blocking=True)
         d_lengths.copy_(h_lengths, non_blocking=True)
-        pkg.topk_ragged(d_scores, d_starts, d_lengths, k, w.offset_mode, out_idx=d_out)
+        pkg.topk_ragged(d_scores, d_starts, d_lengths, k, mode, out_idx=d_out,
+                        page_table=page_table, page_size=max(args.page_size, 1))
         h_out.copy_(d_out, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -397,7 +413,7 @@ def run_ours(args, rank, world, local):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
         "data": "synthetic",
         "config": {"workload": w.name, "B": B, "k": k, "sum_len": total,
-                   "offset_mode": w.offset_mode, "scores": "fp32",
+                   "offset_mode": mode, "page_size": args.page_size, "scores": "fp32",
                    "l2": f"{n_copies} rotating input copies ({n_copies * in_bytes / 1e6:.0f} MB"
                          f" > 3x L2 {l2 / 1e6:.0f} MB): cold scores every step",
                    "timing": "CUDA events around graph replays of K launches on one stream",

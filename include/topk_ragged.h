@@ -119,6 +119,31 @@ int topk_ragged(const float *scores, int64_t n_scores, const int32_t *row_starts
                 int32_t *out_idx, float *out_val, void *stream);
 
 /*
+ * topk_ragged with every selected index written as a KV-cache slot through a
+ * page table: the transform both engines on the pages run right after the
+ * selection (vLLM PR #55872 calls FlashInfer's top_k_ragged_transform;
+ * sglang PR #31115's Modifications note that its selection-only backends
+ * leave out the fused page-table transforms).  Row i's selected in-row index
+ * j is written as
+ *     page_table[i * page_table_stride + j / page_size] * page_size
+ *         + j % page_size,
+ * in canonical order, then -1.
+ *
+ * flags              0 or TOPK_EXCLUDE_NEG_INF (a row-start offset has no
+ *                    meaning here and is rejected).
+ * page_table         device, int32: row i's pages start at
+ *                    page_table + i * page_table_stride and must number at
+ *                    least ceil(L_i / page_size); every slot must fit int32.
+ * page_table_stride  >= 0 (0: all rows read one page table).
+ * page_size          >= 1.
+ * Everything else as for topk_ragged, with the same return codes.
+ */
+int topk_ragged_paged(const float *scores, int64_t n_scores, const int32_t *row_starts,
+                      const int32_t *lengths, int32_t B, int32_t k, int32_t flags,
+                      const int32_t *page_table, int64_t page_table_stride, int32_t page_size,
+                      int32_t *out_idx, float *out_val, void *stream);
+
+/*
  * Reads the current device's status word (an OR of TOPK_DEV_* bits from all
  * calls since the last read) into *host_out, then clears it.  Synchronizes
  * `stream`; not for use under stream capture.  Returns TOPK_OK,

@@ -103,3 +103,17 @@ def topk_ragged(scores: np.ndarray, row_starts: np.ndarray, lengths: np.ndarray,
     if rc != 0:
         raise MemoryError("oracle: worker allocation failed")
     return out_idx, out_val, flags
+
+
+def paged_slots(out_idx: np.ndarray, page_table: np.ndarray, page_size: int) -> np.ndarray:
+    """The page-table transform written out: row i's selected in-row index j
+    becomes page_table[i, j // page_size] * page_size + j % page_size, and -1
+    stays -1.  page_table is [B, P], or [P] shared by every row."""
+    out_idx = np.asarray(out_idx, dtype=np.int64)
+    pt = np.asarray(page_table, dtype=np.int64)
+    if pt.ndim == 1:
+        pt = np.broadcast_to(pt, (out_idx.shape[0], pt.size))
+    j = np.maximum(out_idx, 0)
+    rows = np.arange(out_idx.shape[0])[:, None]
+    slots = pt[rows, j // page_size] * page_size + j % page_size
+    return np.where(out_idx >= 0, slots, -1).astype(np.int32)

@@ -57,11 +57,17 @@ def init(device=None) -> None:
 def topk_ragged(scores: torch.Tensor, row_starts: torch.Tensor, lengths: torch.Tensor,
                 k: int = 2048, offset_mode: int = TOPK_OFFSET_ROW_LOCAL,
                 out_idx: torch.Tensor | None = None, out_val: torch.Tensor | None = None,
-                with_values: bool = False, stream=None):
+                with_values: bool = False, stream=None, page_table: torch.Tensor | None = None,
+                page_size: int = 1):
     """Deterministic exact top-k of each ragged row of a flat fp32 buffer.
 
     scores      float32 CUDA tensor (any shape, contiguous; used as flat).
     row_starts  int32 CUDA tensor [B]; lengths int32 CUDA tensor [B].
+    page_table  optional int32 CUDA tensor [B, P] (or [P], shared by every
+                row): the selected indices are written as KV-cache slots
+                page_table[i, j // page_size] * page_size + j % page_size
+                (topk_ragged_paged); offset_mode may then only carry
+                TOPK_EXCLUDE_NEG_INF.
     Returns (out_idx int32 [B, k], out_val float32 [B, k] or None).
     """
     _check(scores, "scores", torch.float32)
@@ -83,15 +89,25 @@ def topk_ragged(scores: torch.Tensor, row_starts: torch.Tensor, lengths: torch.T
         _check(out_val, "out_val", torch.float32, dev)
         if out_val.numel() != B * k:
             raise ValueError("out_val must hold B * k entries")
-    with torch.cuda.device(dev):
-        rc = lib().topk_ragged(
-            scores.data_ptr() if scores.numel() else None, scores.numel(),
-            row_starts.data_ptr() if B else None, lengths.data_ptr() if B else None,
-            B, int(k), int(offset_mode), out_idx.data_ptr() if B else None,
-            out_val.data_ptr() if (out_val is not None and B) else None,
+    common = (scores.data_ptr() if scores.numel() else None, scores.numel(),
+              row_starts.data_ptr() if B else None, lengths.data_ptr() if B else None,
+              B, int(k), int(offset_mode))
+    tail = (out_idx.data_ptr() if B else None, out_val.data_ptr() if (out_val is not None and B) else None,
             _stream_handle(dev, stream))
+    with torch.cuda.device(dev):
+        if page_table is None:
+            rc = lib().topk_ragged(*common, *tail)
+            name = "topk_ragged"
+        else:
+            _check(page_table, "page_table", torch.int32, dev)
+            stride = page_table.shape[-1] if page_table.dim() == 2 else 0
+            if page_table.dim() == 2 and page_table.shape[0] != B:
+                raise ValueError("page_table must have one row per query row (or be 1-D)")
+            rc = lib().topk_ragged_paged(*common, page_table.data_ptr() if page_table.numel() else None,
+                                         stride, int(page_size), *tail)
+            name = "topk_ragged_paged"
     if rc != 0:
-        raise TopkError(rc, "topk_ragged")
+        raise TopkError(rc, name)
     return out_idx, out_val
 
 

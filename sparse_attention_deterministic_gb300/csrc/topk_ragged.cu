@@ -59,6 +59,10 @@ struct Params {
     int32_t win_cap;     // winner slots in the leader (power of two >= k - 1)
     int32_t off_win;     // byte offset of the winner array in dynamic smem
     int32_t off_keys;    // byte offset of the staged keys in dynamic smem
+    const int32_t *page_table;   // null, or B rows of pt_stride page numbers
+    int64_t pt_stride;
+    int32_t page_size;
+    int32_t page_shift;          // log2(page_size) when a power of two, else -1
 };
 
 // Per-CTA control block at the start of dynamic shared memory.
@@ -748,6 +752,65 @@ __device__ bool short_row(Ctrl &ctrl, uint32_t *cur, uint64_t *buf, uint32_t buf
     return true;
 }
 
+// The page-table transform of a finished output row, in place: every
+// in-row index j becomes pages[j / page_size] * page_size + j % page_size
+// (-1 stays -1).  The caller makes the row's writes visible first.
+// One in-row index through the page table (-1 stays -1).  Slots fit int32
+// by contract, so 32-bit arithmetic is exact.
+template <bool POW2>
+__device__ __forceinline__ int32_t page_slot(int32_t j, const int32_t *pages, int32_t page_size, int32_t page_shift)
+{
+    if (j < 0) return j;
+    if (POW2)
+        return (int32_t)(((uint32_t)__ldg(pages + (j >> page_shift)) << page_shift) | (uint32_t)(j & (page_size - 1)));
+    const int32_t pg = j / page_size;
+    return __ldg(pages + pg) * page_size + (j - pg * page_size);
+}
+
+// The row's first n entries through the page table, four per 16-byte access
+// when the row is 16-byte aligned (the entries from n up to the next
+// multiple of four are -1 padding when k is a multiple of four), two
+// accesses in flight per thread.
+template <bool POW2>
+__device__ __forceinline__ void page_map_entries(int32_t *oi, int n, int k, const int32_t *pages, int32_t page_size,
+                                                 int32_t page_shift)
+{
+    const int nt = (int)blockDim.x;
+    if ((k & 3) == 0 && ((uintptr_t)oi & 15u) == 0) {
+        int4 *o4 = reinterpret_cast<int4 *>(oi);
+        const int nq = (n + 3) >> 2;
+        for (int q0 = (int)threadIdx.x; q0 < nq; q0 += 2 * nt) {
+            int4 v[2];
+#pragma unroll
+            for (int u = 0; u < 2; ++u) v[u] = q0 + u * nt < nq ? o4[q0 + u * nt] : make_int4(-1, -1, -1, -1);
+#pragma unroll
+            for (int u = 0; u < 2; ++u) {
+                v[u].x = page_slot<POW2>(v[u].x, pages, page_size, page_shift);
+                v[u].y = page_slot<POW2>(v[u].y, pages, page_size, page_shift);
+                v[u].z = page_slot<POW2>(v[u].z, pages, page_size, page_shift);
+                v[u].w = page_slot<POW2>(v[u].w, pages, page_size, page_shift);
+            }
+#pragma unroll
+            for (int u = 0; u < 2; ++u)
+                if (q0 + u * nt < nq) o4[q0 + u * nt] = v[u];
+        }
+        return;
+    }
+    for (int q = (int)threadIdx.x; q < n; q += nt) oi[q] = page_slot<POW2>(oi[q], pages, page_size, page_shift);
+}
+
+// The page-table transform of a finished output row, in place: every
+// in-row index j becomes pages[j / page_size] * page_size + j % page_size.
+// The caller makes the row's writes visible to the CTA first.
+__device__ __forceinline__ void page_map_row(const Params &p, int row, int32_t *oi, int n)
+{
+    const int32_t *pages = p.page_table + (int64_t)row * p.pt_stride;
+    if (p.page_shift >= 0)
+        page_map_entries<true>(oi, n, p.k, pages, p.page_size, p.page_shift);
+    else
+        page_map_entries<false>(oi, n, p.k, pages, p.page_size, p.page_shift);
+}
+
 // Quads of warp `warp`'s contiguous segment of the slice.
 struct WarpSeg {
     int q0, q1;
@@ -951,7 +1014,13 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_row_kernel(c
     }
     if (s.nq <= kShortQuads * THREADS) {
         const uint32_t cap = (uint32_t)(p.off_keys + p.stage_cap * 4 - p.off_win) / 8u;
-        if (short_row<THREADS>(ctrl, hist, win, cap, s, k_eff, idx_offset, oi, ov, p.k, excl)) return;
+        if (short_row<THREADS>(ctrl, hist, win, cap, s, k_eff, idx_offset, oi, ov, p.k, excl)) {
+            if (p.page_table) {
+                __syncthreads();
+                page_map_row(p, row, oi, (int)k_eff);
+            }
+            return;
+        }
     }
     const WarpSeg seg = warp_segment<THREADS>(s.nq, warp);
 
@@ -1252,6 +1321,10 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_row_kernel(c
                                 ctrl.wmin, ctrl.kmax, hist, ctrl.scan64, oi, ov, idx_offset, excl);
     }
     pad_out(oi, ov, (int)k_eff, p.k);
+    if (p.page_table) {
+        __syncthreads();
+        page_map_row(p, row, oi, (int)k_eff);
+    }
 }
 
 // ------------------------------------------------------------------------- //
@@ -2090,6 +2163,10 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
                                     ctrl.scan64, oi, ov, idx_offset, excl);
         }
         pad_out(oi, ov, (int)k_eff, p.k);
+        if (p.page_table) {   // the peers' tie writes are visible since B3
+            __syncthreads();
+            page_map_row(p, row, oi, (int)k_eff);
+        }
     }
     cluster_wait();
 }
@@ -2352,18 +2429,16 @@ int topk_ragged_launch_info(int64_t n_scores, int32_t B, int32_t k, topk_launch_
     return TOPK_OK;
 }
 
-int topk_ragged(const float *scores, int64_t n_scores, const int32_t *row_starts,
-                const int32_t *lengths, int32_t B, int32_t k, int32_t offset_mode,
-                int32_t *out_idx, float *out_val, void *stream)
+static int launch(const float *scores, int64_t n_scores, const int32_t *row_starts, const int32_t *lengths,
+                  int32_t B, int32_t k, int32_t offset_mode, const int32_t *page_table, int64_t pt_stride,
+                  int32_t page_size, int32_t *out_idx, float *out_val, void *stream)
 {
-    int rc = validate(scores, n_scores, row_starts, lengths, B, k, offset_mode, out_idx);
-    if (rc != TOPK_OK || B == 0) return rc;
     cudaStream_t st = (cudaStream_t)stream;
     int device = 0;
     if (cudaGetDevice(&device) != cudaSuccess) return TOPK_ERR_CUDA;
     cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
     if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return TOPK_ERR_CUDA;
-    rc = ensure_init(device, cap == cudaStreamCaptureStatusNone);
+    int rc = ensure_init(device, cap == cudaStreamCaptureStatusNone);
     if (rc != TOPK_OK) return rc;
     const Plan pl = make_plan(n_scores, B, k, g_devices[device]);
 
@@ -2381,6 +2456,10 @@ int topk_ragged(const float *scores, int64_t n_scores, const int32_t *row_starts
     prm.win_cap = pl.win_cap;
     prm.off_win = pl.off_win;
     prm.off_keys = pl.off_keys;
+    prm.page_table = page_table;
+    prm.pt_stride = pt_stride;
+    prm.page_size = page_size;
+    prm.page_shift = (page_size & (page_size - 1)) == 0 ? __builtin_ctz((unsigned)page_size) : -1;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)pl.grid, 1, 1);
@@ -2401,6 +2480,30 @@ int topk_ragged(const float *scores, int64_t n_scores, const int32_t *row_starts
         return TOPK_ERR_CUDA;
     }
     return TOPK_OK;
+}
+
+int topk_ragged(const float *scores, int64_t n_scores, const int32_t *row_starts,
+                const int32_t *lengths, int32_t B, int32_t k, int32_t offset_mode,
+                int32_t *out_idx, float *out_val, void *stream)
+{
+    const int rc = validate(scores, n_scores, row_starts, lengths, B, k, offset_mode, out_idx);
+    if (rc != TOPK_OK || B == 0) return rc;
+    return launch(scores, n_scores, row_starts, lengths, B, k, offset_mode, nullptr, 0, 1, out_idx, out_val,
+                  stream);
+}
+
+int topk_ragged_paged(const float *scores, int64_t n_scores, const int32_t *row_starts,
+                      const int32_t *lengths, int32_t B, int32_t k, int32_t flags,
+                      const int32_t *page_table, int64_t page_table_stride, int32_t page_size,
+                      int32_t *out_idx, float *out_val, void *stream)
+{
+    if ((flags & ~TOPK_EXCLUDE_NEG_INF) != 0 || page_size < 1 || page_table_stride < 0)
+        return TOPK_ERR_INVALID_ARG;
+    const int rc = validate(scores, n_scores, row_starts, lengths, B, k, flags, out_idx);
+    if (rc != TOPK_OK || B == 0) return rc;
+    if (!page_table) return TOPK_ERR_INVALID_ARG;
+    return launch(scores, n_scores, row_starts, lengths, B, k, flags, page_table, page_table_stride, page_size,
+                  out_idx, out_val, stream);
 }
 
 int topk_ragged_device_status(uint32_t *host_out, void *stream)

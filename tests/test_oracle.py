@@ -399,6 +399,27 @@ def test_exclusion_equals_selection_of_the_kept_entries(mode):
 
 
 # --------------------------------------------------------------------------- #
+# The page-table transform (the KV-cache slot of each selected index).
+# --------------------------------------------------------------------------- #
+
+def test_paged_slots_hand_case():
+    # Selected [5, 0, 3, -1], pages of 2 entries, row pages [7, 2, 9]:
+    # 5 -> page 9 offset 1 = 19; 0 -> page 7 offset 0 = 14; 3 -> page 2
+    # offset 1 = 5.
+    got = oracle.paged_slots(np.array([[5, 0, 3, -1]]), np.array([[7, 2, 9]]), 2)
+    assert got.tolist() == [[19, 14, 5, -1]]
+
+
+def test_paged_slots_identity_and_shared_table():
+    rng = np.random.default_rng(3)
+    idx = np.where(rng.random((4, 50)) < 0.2, -1, rng.integers(0, 64, (4, 50)))
+    # One entry per page and pages 0, 1, 2, ...: slots are the indices.
+    assert (oracle.paged_slots(idx, np.arange(64), 1) == idx).all()
+    # 16 entries per page, identity pages: still the indices.
+    assert (oracle.paged_slots(idx, np.tile(np.arange(4), (4, 1)), 16) == idx).all()
+
+
+# --------------------------------------------------------------------------- #
 # Invariants on arbitrary bit patterns, and thread-count independence.
 # --------------------------------------------------------------------------- #
 
