@@ -117,3 +117,64 @@ def paged_slots(out_idx: np.ndarray, page_table: np.ndarray, page_size: int) -> 
     rows = np.arange(out_idx.shape[0])[:, None]
     slots = pt[rows, j // page_size] * page_size + j % page_size
     return np.where(out_idx >= 0, slots, -1).astype(np.int32)
+
+
+# --- tie / plateau statistics at the k-th boundary ----------------------------
+# Fields of one row of row_stats(), in order.
+ROW_STATS_FIELDS = ("len", "n_zero", "boundary_bits", "tie", "above", "flags")
+STAT_HAS_BOUNDARY = 1   # L > k: the row has a k-th entry
+STAT_STRADDLE = 2       # the tie set of the boundary crosses position k
+STAT_ZERO_BOUND = 4     # the boundary score is 0.0 (either sign)
+MAX_LEN = 1 << 24
+
+
+def row_stats(scores: np.ndarray, row_starts: np.ndarray, lengths: np.ndarray, k: int):
+    """Per-row statistics of the k-th boundary, as the sglang page's score
+    statistics script defines them (its row_stats: plateau fraction, the k-th
+    largest score, the size of its tie set, the count strictly above it, and
+    whether the tie set straddles position k or the boundary sits on 0.0),
+    written out on the same bitwise order as the selection (C1, C2): the
+    boundary is the k-th entry in canonical order, "tie" counts the entries
+    bitwise equal to it and "above" those with a larger order key.  n_zero
+    counts the entries whose value is 0.0 (+0.0 or -0.0).
+
+    A row with L <= k has no boundary: (L, n_zero, 0, 0, L, 0).  Window and
+    length checks are topk_ragged's; a rejected row is all zero and its flag
+    is set in the returned row_flags.
+
+    Returns ``(stats uint32[B, 6] in ROW_STATS_FIELDS order, row_flags uint32[B])``.
+    """
+    if not 1 <= k <= 4096:
+        raise ValueError(f"k={k} outside [1, 4096]")
+    bits = np.ascontiguousarray(scores, dtype=np.float32).reshape(-1).view(np.uint32)
+    row_starts = np.asarray(row_starts, dtype=np.int64).reshape(-1)
+    lengths = np.asarray(lengths, dtype=np.int64).reshape(-1)
+    B = row_starts.size
+    out = np.zeros((B, 6), dtype=np.uint32)
+    row_flags = np.zeros(B, dtype=np.uint32)
+    for i in range(B):
+        L = max(int(lengths[i]), 0)
+        s0 = int(row_starts[i])
+        if L >= MAX_LEN:
+            row_flags[i] = FLAG_LEN_ENVELOPE
+            continue
+        if s0 < 0 or s0 + L > bits.size:
+            row_flags[i] = FLAG_BAD_WINDOW
+            continue
+        b = bits[s0:s0 + L]
+        n_zero = int(np.count_nonzero((b & 0x7FFFFFFF) == 0))
+        if L <= k:
+            out[i] = (L, n_zero, 0, 0, L, 0)
+            continue
+        key = order_key(b)
+        T = np.sort(key)[::-1][k - 1]          # the k-th key in canonical order
+        tie = int(np.count_nonzero(key == T))
+        above = int(np.count_nonzero(key > T))
+        bb = int(b[np.flatnonzero(key == T)[0]])   # the key is a bijection: one pattern
+        flags = STAT_HAS_BOUNDARY
+        if tie > 1 and above + tie > k:
+            flags |= STAT_STRADDLE
+        if bb & 0x7FFFFFFF == 0:
+            flags |= STAT_ZERO_BOUND
+        out[i] = (L, n_zero, bb, tie, above, flags)
+    return out, row_flags
