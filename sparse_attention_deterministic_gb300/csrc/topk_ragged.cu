@@ -63,6 +63,7 @@ struct Params {
     int64_t pt_stride;
     int32_t page_size;
     int32_t page_shift;          // log2(page_size) when a power of two, else -1
+    int32_t ahead;               // row kernel: L2 prefetch distance in rows (0: none)
 };
 
 // Per-CTA control block at the start of dynamic shared memory.
@@ -955,8 +956,10 @@ __device__ RowGroup assign_rows(const Params &p, uint32_t crank, uint32_t csize,
 // quads per lane in flight, so per-warp counts taken in one pass give
 // index-ordered positions in a later one.
 // ------------------------------------------------------------------------- //
+// Five CTAs per SM (48 registers, a few bytes spilled): five rows in flight
+// per SM ran faster than four at 64 registers.
 template <int THREADS>
-__global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_row_kernel(const Params p)
+__global__ void __launch_bounds__(THREADS, 5) topk_row_kernel(const Params p)
 {
     constexpr int NW = THREADS / 32;
     constexpr int U = 4;                       // quads in flight per lane
@@ -974,6 +977,14 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_row_kernel(c
     // ---- a1: metadata, window checks ----------------------------------- //
     const int64_t rs = p.row_starts[row];
     int64_t len = p.lengths[row];
+    // The row about one wave of CTAs ahead: its metadata loads along with
+    // this row's, and its scores are prefetched into L2 below, so the CTA
+    // that takes it later finds them there.
+    int64_t rs_a = 0, len_a = 0;
+    if (warp == THREADS / 32 - 1 && row + p.ahead < p.B && p.ahead > 0) {
+        rs_a = p.row_starts[row + p.ahead];
+        len_a = p.lengths[row + p.ahead];
+    }
     if (len < 0) len = 0;
     uint32_t bad = 0;
     if (len >= (int64_t)TOPK_RAGGED_MAX_LEN)
@@ -1011,6 +1022,12 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_row_kernel(c
         s.nq = (s.end + 3) >> 2;
         s.sq = s.nq < (p.stage_cap >> 2) ? s.nq : (p.stage_cap >> 2);
         s.jbase = (int32_t)(sbase - rs);
+    }
+    if (len_a > 0 && rs_a >= 0 && rs_a + len_a <= p.n_scores) {
+        const char *b = reinterpret_cast<const char *>(p.scores + rs_a);
+        const int64_t nbytes = min(len_a * 4, (int64_t)32768);
+        for (int64_t o = (int64_t)lane * 128; o < nbytes; o += 32 * 128)
+            asm volatile("prefetch.global.L2 [%0];" ::"l"(b + o));
     }
     if (s.nq <= kShortQuads * THREADS) {
         const uint32_t cap = (uint32_t)(p.off_keys + p.stage_cap * 4 - p.off_win) / 8u;
@@ -2172,6 +2189,157 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
 }
 
 // ------------------------------------------------------------------------- //
+// Tie / plateau statistics of each row at its k-th boundary, one CTA per
+// row.  The radix select of the top-k kernels, with every pass reading the
+// row from global memory: the top 11, next 11 and last 10 bits of the order
+// key narrow the bin holding the k-th key down to the key itself, and the
+// entries above it and equal to it are the counts above and inside the last
+// bin.  A row no longer than k takes one pass (its 0.0 count).
+// ------------------------------------------------------------------------- //
+constexpr int kStatsThreads = 512;
+
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS) topk_stats_kernel(const float *scores, int64_t n_scores,
+                                                             const int32_t *row_starts, const int32_t *lengths,
+                                                             int32_t k, topk_row_stats *out)
+{
+    constexpr int BPT = kBins / THREADS;
+    constexpr uint32_t kNone = 0xFFFFFFFFu;
+    __shared__ uint32_t hist[kBins];
+    __shared__ uint32_t scan[32];
+    __shared__ uint32_t sel[3];   // selected digit, entries above its bin, 0.0 count
+    const int tid = threadIdx.x, lane = tid & 31;
+    const int row = (int)blockIdx.x;
+
+    topk_row_stats res = {0u, 0u, 0u, 0u, 0u, 0u};
+    const int64_t rs = row_starts[row];
+    int64_t len = lengths[row];
+    if (len < 0) len = 0;
+    uint32_t bad = 0;
+    if (len >= (int64_t)TOPK_RAGGED_MAX_LEN)
+        bad = TOPK_DEV_LEN_ENVELOPE;
+    else if (rs < 0 || rs + len > n_scores)
+        bad = TOPK_DEV_BAD_WINDOW;
+    if (bad) {
+        if (tid == 0) {
+            atomicOr(&g_status, bad);
+            out[row] = res;
+        }
+        return;
+    }
+    const uint32_t L = (uint32_t)len;
+    const bool has_boundary = L > (uint32_t)k;
+
+    // The row as [head | 16-byte aligned quads | tail]; head and tail hold
+    // fewer than four entries each.
+    const float *x = scores + rs;
+    const uint32_t *xs = reinterpret_cast<const uint32_t *>(x);
+    const uint32_t head = min(L, (4u - (uint32_t)(((uintptr_t)x >> 2) & 3u)) & 3u);
+    const uint32_t nq = (L - head) >> 2;
+    const uint32_t tail0 = head + 4u * nq;
+    const uint4 *xq = reinterpret_cast<const uint4 *>(x + head);
+
+    uint32_t prefix = 0, above = 0, r = (uint32_t)k, tie = 0;
+    const int levels = has_boundary ? 3 : 1;
+    for (int level = 0; level < levels; ++level) {
+        const int dsh = level == 0 ? 21 : (level == 1 ? 10 : 0);   // digit shift
+        const int dbits = level == 2 ? 10 : 11;
+        const uint32_t dmask = (1u << dbits) - 1u;
+        for (int b = tid; b < kBins; b += THREADS) hist[b] = 0u;
+        if (tid == 0) {
+            sel[0] = kNone;
+            sel[1] = 0u;
+            if (level == 0) sel[2] = 0u;
+        }
+        __syncthreads();
+
+        // Level 0 counts 0.0 entries and bins every entry; later levels bin
+        // the entries whose higher bits equal the selected prefix.
+        uint32_t nz = 0;
+        auto visit = [&](uint32_t u) {
+            const uint32_t key = order_key(u);
+            if (level == 0) {
+                nz += (u & 0x7FFFFFFFu) == 0u;
+                if (has_boundary) atomicAdd(&hist[key >> 21], 1u);
+            } else if ((key >> (dsh + dbits)) == prefix) {
+                atomicAdd(&hist[(key >> dsh) & dmask], 1u);
+            }
+        };
+        if ((uint32_t)tid < head) visit(xs[tid]);
+        for (uint32_t q = (uint32_t)tid; q < nq; q += 4u * THREADS) {
+            uint4 v[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                v[t] = q + t * THREADS < nq ? __ldg(xq + q + t * THREADS) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                if (q + t * THREADS < nq) {
+                    visit(v[t].x);
+                    visit(v[t].y);
+                    visit(v[t].z);
+                    visit(v[t].w);
+                }
+            }
+        }
+        if (tail0 + (uint32_t)tid < L) visit(xs[tail0 + tid]);
+        if (level == 0) {
+            nz = __reduce_add_sync(kFull, nz);
+            if (lane == 0 && nz) atomicAdd(&sel[2], nz);
+        }
+        __syncthreads();
+        if (!has_boundary) break;
+
+        // The bin where the count from the top first reaches r; thread t
+        // holds bins kBins-1-BPT*t down to kBins-BPT*(t+1).
+        uint32_t h[BPT], sum = 0;
+#pragma unroll
+        for (int i = 0; i < BPT; ++i) {
+            h[i] = hist[kBins - 1 - (BPT * tid + i)];
+            sum += h[i];
+        }
+        uint32_t run = block_incl_scan<THREADS>(sum, scan) - sum;
+#pragma unroll
+        for (int i = 0; i < BPT; ++i) {
+            if (run < r && run + h[i] >= r) {
+                sel[0] = (uint32_t)(kBins - 1 - (BPT * tid + i));
+                sel[1] = run;
+            }
+            run += h[i];
+        }
+        __syncthreads();
+        const uint32_t d = sel[0];
+        if (d == kNone) {   // cannot happen: the selected bin always holds >= r entries
+            if (tid == 0) {
+                atomicOr(&g_status, TOPK_DEV_INTERNAL);
+                out[row] = res;
+            }
+            return;
+        }
+        above += sel[1];
+        r -= sel[1];
+        prefix = (prefix << dbits) | d;
+        if (level == 2) tie = hist[d];
+        __syncthreads();   // every thread has read sel and hist
+    }
+    if (tid == 0) {
+        res.len = L;
+        res.n_zero = sel[2];
+        if (has_boundary) {
+            const uint32_t T = prefix;   // the k-th key
+            res.boundary_bits = key_bits(T);
+            res.tie = tie;
+            res.above = above;
+            res.flags = TOPK_STAT_HAS_BOUNDARY;
+            if (tie > 1u && above + tie > (uint32_t)k) res.flags |= TOPK_STAT_STRADDLE;
+            if ((res.boundary_bits & 0x7FFFFFFFu) == 0u) res.flags |= TOPK_STAT_ZERO_BOUND;
+        } else {
+            res.above = L;
+        }
+        out[row] = res;
+    }
+}
+
+// ------------------------------------------------------------------------- //
 // Host side.
 // ------------------------------------------------------------------------- //
 typedef void (*KernelFn)(const Params);
@@ -2459,6 +2627,7 @@ static int launch(const float *scores, int64_t n_scores, const int32_t *row_star
     prm.page_table = page_table;
     prm.pt_stride = pt_stride;
     prm.page_size = page_size;
+    prm.ahead = pl.v->cluster ? 0 : g_devices[device].sm_count * 5;
     prm.page_shift = (page_size & (page_size - 1)) == 0 ? __builtin_ctz((unsigned)page_size) : -1;
 
     cudaLaunchConfig_t cfg = {};
@@ -2504,6 +2673,35 @@ int topk_ragged_paged(const float *scores, int64_t n_scores, const int32_t *row_
     if (!page_table) return TOPK_ERR_INVALID_ARG;
     return launch(scores, n_scores, row_starts, lengths, B, k, flags, page_table, page_table_stride, page_size,
                   out_idx, out_val, stream);
+}
+
+int topk_ragged_stats(const float *scores, int64_t n_scores, const int32_t *row_starts,
+                      const int32_t *lengths, int32_t B, int32_t k, topk_row_stats *out,
+                      void *stream)
+{
+    if (k < 1 || k > TOPK_RAGGED_MAX_K || B < 0) return TOPK_ERR_INVALID_ARG;
+    if (n_scores < 0 || n_scores >= ((int64_t)1 << 31)) return TOPK_ERR_INVALID_ARG;
+    if (B == 0) return TOPK_OK;
+    if (!row_starts || !lengths || !out) return TOPK_ERR_INVALID_ARG;
+    if (!scores && n_scores > 0) return TOPK_ERR_INVALID_ARG;
+    if (((uintptr_t)scores & 3u) != 0) return TOPK_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return TOPK_ERR_CUDA;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return TOPK_ERR_CUDA;
+    const int rc = ensure_init(device, cap == cudaStreamCaptureStatusNone);
+    if (rc != TOPK_OK) return rc;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)B, 1, 1);
+    cfg.blockDim = dim3((unsigned)kStatsThreads, 1, 1);
+    cfg.stream = st;
+    if (cudaLaunchKernelEx(&cfg, topk_stats_kernel<kStatsThreads>, scores, n_scores, row_starts, lengths, k,
+                           out) != cudaSuccess) {
+        cudaGetLastError();
+        return TOPK_ERR_CUDA;
+    }
+    return TOPK_OK;
 }
 
 int topk_ragged_device_status(uint32_t *host_out, void *stream)
