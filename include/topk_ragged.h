@@ -32,7 +32,7 @@
 extern "C" {
 #endif
 
-#define TOPK_RAGGED_ABI_VERSION 2
+#define TOPK_RAGGED_ABI_VERSION 3
 #define TOPK_RAGGED_MAX_K 4096
 /* Row lengths must stay below 2^24, the envelope of the 24-bit index field. */
 #define TOPK_RAGGED_MAX_LEN (1 << 24)
@@ -142,6 +142,42 @@ int topk_ragged_paged(const float *scores, int64_t n_scores, const int32_t *row_
                       const int32_t *lengths, int32_t B, int32_t k, int32_t flags,
                       const int32_t *page_table, int64_t page_table_stride, int32_t page_size,
                       int32_t *out_idx, float *out_val, void *stream);
+
+/*
+ * Tie / plateau statistics of one row at its k-th boundary: the per-row
+ * figures of the sglang page's score-statistics script (row_stats: plateau
+ * fraction, the k-th score, its tie set, the count strictly above it,
+ * straddle, zero_bound), taken on the selection's bitwise order.
+ */
+typedef struct {
+    uint32_t len;            /* L_i after clamping (0 for a rejected row)           */
+    uint32_t n_zero;         /* entries whose value is 0.0 (+0.0 or -0.0)          */
+    uint32_t boundary_bits;  /* fp32 bits of the k-th entry in canonical order     */
+    uint32_t tie;            /* entries bitwise equal to the boundary              */
+    uint32_t above;          /* entries above the boundary in the order (L if L<=k)*/
+    uint32_t flags;          /* TOPK_STAT_* bits                                   */
+} topk_row_stats;
+
+enum {
+    TOPK_STAT_HAS_BOUNDARY = 1u, /* L_i > k; otherwise boundary_bits and tie are 0  */
+    TOPK_STAT_STRADDLE = 2u,     /* tie > 1 and above + tie > k: the selection takes
+                                    part of the tie set, by index                   */
+    TOPK_STAT_ZERO_BOUND = 4u    /* the boundary score is 0.0 (either sign)         */
+};
+
+/*
+ * Fills out[i] (device memory, B entries, caller-owned) with the statistics
+ * of row i for this k.  Same inputs, window checks and status bits as
+ * topk_ragged: a row outside [0, n_scores) or with L_i >= 2^24 is written
+ * as all zero and sets its TOPK_DEV_* bit.  One launch, stream-ordered, no
+ * allocation, capturable after topk_ragged_init.  Returns TOPK_OK,
+ * TOPK_ERR_INVALID_ARG (k outside [1, 4096], B < 0, n_scores outside
+ * [0, 2^31), NULL pointers with B > 0, scores not 4-byte aligned),
+ * TOPK_ERR_NOT_INITIALIZED, TOPK_ERR_UNSUPPORTED_DEVICE or TOPK_ERR_CUDA.
+ */
+int topk_ragged_stats(const float *scores, int64_t n_scores, const int32_t *row_starts,
+                      const int32_t *lengths, int32_t B, int32_t k, topk_row_stats *out,
+                      void *stream);
 
 /*
  * Reads the current device's status word (an OR of TOPK_DEV_* bits from all

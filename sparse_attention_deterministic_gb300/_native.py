@@ -26,6 +26,7 @@ EXPORTS = (
     "topk_ragged_init",
     "topk_ragged",
     "topk_ragged_paged",
+    "topk_ragged_stats",
     "topk_ragged_device_status",
     "topk_ragged_launch_info",
 )
@@ -96,6 +97,9 @@ def lib() -> ctypes.CDLL:
                                          ctypes.c_int64, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p,
                                          ctypes.c_void_p]
         so.topk_ragged_paged.restype = ctypes.c_int
+        so.topk_ragged_stats.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
+                                         ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
+        so.topk_ragged_stats.restype = ctypes.c_int
         so.topk_ragged_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_void_p]
         so.topk_ragged_device_status.restype = ctypes.c_int
         so.topk_ragged_launch_info.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,

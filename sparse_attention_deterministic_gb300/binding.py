@@ -20,6 +20,11 @@ TOPK_EXCLUDE_NEG_INF = 2   # or-ed into offset_mode: leave out -inf and negative
 TOPK_DEV_LEN_ENVELOPE = 1
 TOPK_DEV_BAD_WINDOW = 2
 TOPK_DEV_INTERNAL = 4
+# topk_row_stats: six 32-bit fields per row, and its flag bits
+ROW_STATS_FIELDS = ("len", "n_zero", "boundary_bits", "tie", "above", "flags")
+TOPK_STAT_HAS_BOUNDARY = 1
+TOPK_STAT_STRADDLE = 2
+TOPK_STAT_ZERO_BOUND = 4
 MAX_K = 4096
 MAX_LEN = 1 << 24
 PAD_VALUE_BITS = 0xFF800000
@@ -109,6 +114,36 @@ def topk_ragged(scores: torch.Tensor, row_starts: torch.Tensor, lengths: torch.T
     if rc != 0:
         raise TopkError(rc, name)
     return out_idx, out_val
+
+
+def topk_ragged_stats(scores: torch.Tensor, row_starts: torch.Tensor, lengths: torch.Tensor,
+                      k: int = 2048, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Tie / plateau statistics of each row at its k-th boundary.
+
+    Returns an int32 CUDA tensor [B, 6] holding topk_row_stats per row, in
+    ROW_STATS_FIELDS order; every field is an unsigned 32-bit value (read
+    boundary_bits as the fp32 pattern of the k-th score).
+    """
+    _check(scores, "scores", torch.float32)
+    dev = scores.device
+    _check(row_starts, "row_starts", torch.int32, dev)
+    _check(lengths, "lengths", torch.int32, dev)
+    B = row_starts.numel()
+    if lengths.numel() != B:
+        raise ValueError(f"row_starts has {B} entries, lengths has {lengths.numel()}")
+    if out is None:
+        out = torch.empty((B, len(ROW_STATS_FIELDS)), dtype=torch.int32, device=dev)
+    else:
+        _check(out, "out", torch.int32, dev)
+        if out.numel() != B * len(ROW_STATS_FIELDS):
+            raise ValueError("out must hold B * 6 entries")
+    with torch.cuda.device(dev):
+        rc = lib().topk_ragged_stats(scores.data_ptr() if scores.numel() else None, scores.numel(),
+                                     row_starts.data_ptr() if B else None, lengths.data_ptr() if B else None,
+                                     B, int(k), out.data_ptr() if B else None, _stream_handle(dev, stream))
+    if rc != 0:
+        raise TopkError(rc, "topk_ragged_stats")
+    return out
 
 
 def device_status(device=None, stream=None) -> int:

@@ -39,7 +39,7 @@ def test_exports_every_declared_symbol(so):
 
 
 def test_abi_version_and_strerror(so):
-    assert so.topk_ragged_abi_version() == 2
+    assert so.topk_ragged_abi_version() == 3
     for st in range(5):
         assert pkg.strerror(st)
     assert pkg.strerror(99) == "unknown status"
@@ -57,6 +57,27 @@ def _call(so, scores=0x1000, n=16, rs=0x2000, ln=0x3000, B=1, k=4, mode=0, oi=0x
 def test_invalid_arguments_rejected_on_host(so, kw):
     # Pointers here are never dereferenced: validation fails first.
     assert _call(so, **kw) == 1
+
+
+@pytest.mark.parametrize("args", [
+    (0x1000, 16, 0x2000, 0x3000, 1, 0, 0x4000), (0x1000, 16, 0x2000, 0x3000, 1, 4097, 0x4000),
+    (0x1000, 16, 0x2000, 0x3000, -1, 4, 0x4000), (0x1000, 16, None, 0x3000, 1, 4, 0x4000),
+    (0x1000, 16, 0x2000, None, 1, 4, 0x4000), (0x1000, 16, 0x2000, 0x3000, 1, 4, None),
+    (None, 16, 0x2000, 0x3000, 1, 4, 0x4000), (0x1002, 16, 0x2000, 0x3000, 1, 4, 0x4000),
+    (0x1000, -1, 0x2000, 0x3000, 1, 4, 0x4000), (0x1000, 1 << 31, 0x2000, 0x3000, 1, 4, 0x4000),
+])
+def test_stats_invalid_arguments_rejected_on_host(so, args):
+    assert so.topk_ragged_stats(*args, None) == 1
+
+
+def test_stats_empty_batch_and_header_flags(so):
+    assert so.topk_ragged_stats(None, 0, None, None, 0, 2048, None, None) == 0
+    text = open(os.path.join(ROOT, "include", "topk_ragged.h")).read()
+    assert re.search(r"TOPK_STAT_HAS_BOUNDARY = 1u", text) and pkg.TOPK_STAT_HAS_BOUNDARY == 1
+    assert re.search(r"TOPK_STAT_STRADDLE = 2u", text) and pkg.TOPK_STAT_STRADDLE == 2
+    assert re.search(r"TOPK_STAT_ZERO_BOUND = 4u", text) and pkg.TOPK_STAT_ZERO_BOUND == 4
+    fields = re.search(r"typedef struct \{(.*?)\} topk_row_stats;", text, re.S).group(1)
+    assert re.findall(r"uint32_t (\w+);", fields) == list(pkg.ROW_STATS_FIELDS)
 
 
 def test_empty_batch_is_ok_without_device(so):
