@@ -1,6 +1,7 @@
 """Benchmark: deterministic exact ragged top-k on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
+                    [--page-size P] [--op topk|stats]
 
 A step is one call of the whole hot path (one launch of the library over one
 batch of rows).  The default workload is the decode batch: 64 rows with
@@ -8,6 +9,10 @@ lengths uniform in [4096, 131072], lightning-indexer scores, k = 2048.  The
 timed region replays the K launches from CUDA graphs over rotating input
 copies whose total exceeds 3x the L2 size, so every step reads cold scores
 from HBM.  Rank 0 prints one JSON line.
+
+--page-size P times the page-table transform (topk_ragged_paged) and
+--op stats the tie / plateau statistics op (topk_ragged_stats) on the same
+workload, in the same way.
 
 --impl reference times the CPU oracle (the plain per-row sort the library is
 checked against) on the host cores, on a bounded sample of rows per step.
@@ -30,6 +35,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 METRIC = "ragged exact top-k rows/s and achieved HBM GB/s (k=2048) vs roofline"
+METRIC_STATS = "ragged tie/plateau statistics rows/s and achieved HBM GB/s (k=2048) vs roofline"
+STATS_FIELDS = 6   # 32-bit fields of one topk_row_stats
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
 KERNEL_SRC = os.path.join(ROOT, "sparse_attention_deterministic_gb300", "csrc", "topk_ragged.cu")
@@ -53,6 +60,8 @@ def parse_args():
     p.add_argument("--page-size", type=int, default=0,
                    help="write KV-cache slots through random per-row page tables of this "
                         "page size (topk_ragged_paged); 0: plain indices")
+    p.add_argument("--op", default="topk", choices=["topk", "stats"],
+                   help="topk: the selection; stats: per-row tie/plateau statistics")
     return p.parse_args()
 
 
@@ -83,6 +92,11 @@ def whole_job_rate(units_per_rank: float, ms_per_step: float, world: int) -> flo
 def algorithmic_bytes(total_len: int, B: int, k: int) -> int:
     """One read of every score, the index writes and the row metadata."""
     return 4 * total_len + 4 * B * k + 8 * B
+
+
+def algorithmic_bytes_stats(total_len: int, B: int) -> int:
+    """One read of every score, the row metadata and the statistics written."""
+    return 4 * total_len + 8 * B + 4 * STATS_FIELDS * B
 
 
 def kernel_source_sha() -> str:
@@ -169,7 +183,7 @@ class ClockSampler:
 # CPU oracle arm (also the cpu_baseline key of our arm).
 # --------------------------------------------------------------------------- #
 
-def time_oracle(w, seconds: float, rows_per_call=None, max_calls=None):
+def time_oracle(w, seconds: float, rows_per_call=None, max_calls=None, op="topk"):
     """Run the oracle on row samples of the workload for about `seconds`.
     Returns (rows/s, elements/s, threads, description)."""
     import numpy as np
@@ -187,8 +201,12 @@ def time_oracle(w, seconds: float, rows_per_call=None, max_calls=None):
     while True:
         sel = (np.arange(cursor, cursor + rows_per_call) % B)
         cursor = (cursor + rows_per_call) % B
-        oracle.topk_ragged(s, st[sel], ln[sel], w.k, w.offset_mode, n_threads=threads,
-                           with_values=False)
+        if op == "stats":
+            threads = 1
+            oracle.row_stats(s, st[sel], ln[sel], w.k)
+        else:
+            oracle.topk_ragged(s, st[sel], ln[sel], w.k, w.offset_mode, n_threads=threads,
+                               with_values=False)
         rows += rows_per_call
         elems += int(ln[sel].clip(min=0).sum())
         calls += 1
@@ -217,22 +235,30 @@ def run_reference(args, rank):
     cores = len(os.sched_getaffinity(0))
     # Calibrate one row's single-thread cost over the length mix, then size
     # every step so the whole run ends in about two minutes.
+    stats = args.op == "stats"
+
+    def run_oracle(sel, n_threads):
+        if stats:   # a Python loop over rows: one thread
+            oracle.row_stats(s, st[sel], ln[sel], w.k)
+        else:
+            oracle.topk_ragged(s, st[sel], ln[sel], w.k, w.offset_mode, n_threads=n_threads,
+                               with_values=False)
+
     probe = np.linspace(0, w.B - 1, num=min(w.B, 8)).astype(np.int64)
     t0 = time.perf_counter()
-    oracle.topk_ragged(s, st[probe], ln[probe], w.k, w.offset_mode, n_threads=1,
-                       with_values=False)
+    run_oracle(probe, 1)
     per_row_s = (time.perf_counter() - t0) / len(probe)
     budget_s = 120.0 / max(1, args.steps + args.warmup)
-    rows_per_step = max(1, min(w.B, int(budget_s / max(per_row_s, 1e-9) * cores)))
-    threads = max(1, min(cores, rows_per_step))
+    par = 1 if stats else cores
+    rows_per_step = max(1, min(w.B, int(budget_s / max(per_row_s, 1e-9) * par)))
+    threads = 1 if stats else max(1, min(cores, rows_per_step))
     cursor = 0
 
     def step():
         nonlocal cursor
         sel = np.arange(cursor, cursor + rows_per_step) % w.B
         cursor = (cursor + rows_per_step) % w.B
-        oracle.topk_ragged(s, st[sel], ln[sel], w.k, w.offset_mode, n_threads=threads,
-                           with_values=False)
+        run_oracle(sel, threads)
         return int(ln[sel].clip(min=0).sum())
 
     for _ in range(args.warmup):
@@ -245,12 +271,12 @@ def run_reference(args, rank):
     rows = rows_per_step * args.steps
     value = rows / el
     line = {
-        "impl": "reference", "metric": METRIC, "value": value, "unit": "rows/s",
+        "impl": "reference", "metric": METRIC_STATS if stats else METRIC, "value": value, "unit": "rows/s",
         "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * el / args.steps, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "u32", "data": "synthetic",
         "config": {"workload": w.name, "B": w.B, "k": w.k, "sum_len": w.total_len(),
-                   "offset_mode": w.offset_mode, "rows_per_step": rows_per_step},
+                   "offset_mode": w.offset_mode, "rows_per_step": rows_per_step, "op": args.op},
         "cpu_baseline": {"value": value, "unit": "rows/s", "cores": threads, "kind": "oracle",
                          "sample": f"{rows_per_step} row(s) of the {w.name} workload per step, "
                                    f"rows cycled in order; {elems} scores in {el:.2f} s"},
@@ -281,13 +307,18 @@ def run_ours(args, rank, world, local):
 
     w = W.make(args.config, device=device)
     B, k, total = w.B, w.k, w.total_len()
+    stats = args.op == "stats"
+    if stats and args.page_size > 0:
+        raise SystemExit("--page-size applies to --op topk")
+    out_cols = STATS_FIELDS if stats else k
     in_bytes = w.scores.numel() * 4 + 8 * B
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
     n_copies = max(2, math.ceil(3 * l2 / in_bytes) + 1)
     copies = [w.scores.clone() for _ in range(n_copies)]
-    outs = [torch.empty((B, k), dtype=torch.int32, device=device) for _ in range(n_copies)]
+    outs = [torch.empty((B, out_cols), dtype=torch.int32, device=device) for _ in range(n_copies)]
     stream = torch.cuda.Stream(device)
-    info = pkg.launch_info(w.scores.numel(), B, k, device)
+    info = ({"kernel": "topk_stats_kernel", "grid": B, "cluster": 1, "launches": 1 if B else 0}
+            if stats else pkg.launch_info(w.scores.numel(), B, k, device))
 
     # The page-table transform: random per-row page tables (the row-start
     # offset has no meaning there, so the mode keeps only its other bits).
@@ -299,9 +330,15 @@ def run_ours(args, rank, world, local):
                                  ).to(torch.int32).to(device)
         mode = w.offset_mode & ~pkg.TOPK_OFFSET_ROW_START
 
+    def call(scores, starts, lengths, out, s=None):
+        if stats:
+            pkg.topk_ragged_stats(scores, starts, lengths, k, out=out, stream=s)
+        else:
+            pkg.topk_ragged(scores, starts, lengths, k, mode, out_idx=out, stream=s,
+                            page_table=page_table, page_size=max(args.page_size, 1))
+
     def launch(i, s=stream):
-        pkg.topk_ragged(copies[i], w.row_starts, w.lengths, k, mode, out_idx=outs[i], stream=s,
-                        page_table=page_table, page_size=max(args.page_size, 1))
+        call(copies[i], w.row_starts, w.lengths, outs[i], s)
 
     # Parity guard: the timed configuration must match the oracle on this input.
     import numpy as np
@@ -311,8 +348,11 @@ def run_ours(args, rank, world, local):
         launch(0)
     stream.synchronize()
     s_np, st_np, ln_np = w.numpy()
-    ref, _, _ = oracle.topk_ragged(s_np, st_np, ln_np, k, mode,
-                                   n_threads=len(os.sched_getaffinity(0)), with_values=False)
+    if stats:
+        ref = oracle.row_stats(s_np, st_np, ln_np, k)[0].view(np.int32)
+    else:
+        ref, _, _ = oracle.topk_ragged(s_np, st_np, ln_np, k, mode,
+                                       n_threads=len(os.sched_getaffinity(0)), with_values=False)
     if page_table is not None:
         ref = oracle.paged_slots(ref, page_table.cpu().numpy(), args.page_size)
     parity = bool(np.array_equal(outs[0].cpu().numpy(), ref))
@@ -369,18 +409,17 @@ def run_ours(args, rank, world, local):
     h_scores = w.scores.cpu().pin_memory()
     h_starts = w.row_starts.cpu().pin_memory()
     h_lengths = w.lengths.cpu().pin_memory()
-    h_out = torch.empty((B, k), dtype=torch.int32).pin_memory()
+    h_out = torch.empty((B, out_cols), dtype=torch.int32).pin_memory()
     d_scores = torch.empty_like(w.scores)
     d_starts = torch.empty_like(w.row_starts)
     d_lengths = torch.empty_like(w.lengths)
-    d_out = torch.empty((B, k), dtype=torch.int32, device=device)
+    d_out = torch.empty((B, out_cols), dtype=torch.int32, device=device)
 
     def e2e_step():
         d_scores.copy_(h_scores, non_blocking=True)
         d_starts.copy_(h_starts, non_blocking=True)
         d_lengths.copy_(h_lengths, non_blocking=True)
-        pkg.topk_ragged(d_scores, d_starts, d_lengths, k, mode, out_idx=d_out,
-                        page_table=page_table, page_size=max(args.page_size, 1))
+        call(d_scores, d_starts, d_lengths, d_out)
         h_out.copy_(d_out, non_blocking=True)
 
     with torch.cuda.stream(stream):
@@ -400,20 +439,20 @@ def run_ours(args, rank, world, local):
     if rank != 0:
         return
     peak, peak_kind = hbm_peak()
-    alg = algorithmic_bytes(total, B, k)
+    alg = algorithmic_bytes_stats(total, B) if stats else algorithmic_bytes(total, B, k)
     achieved = alg / (ms_per_step * 1e-3) / 1e9
     cpu = None
     if not args.no_cpu_baseline and world == 1:
-        rps, eps, threads, desc = time_oracle(w.to("cpu"), args.cpu_seconds)
+        rps, eps, threads, desc = time_oracle(w.to("cpu"), args.cpu_seconds, op=args.op)
         cpu = {"value": rps, "unit": "rows/s", "cores": threads, "kind": "oracle",
                "sample": desc, "elements_per_s": eps}
     line = {
-        "metric": METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
+        "metric": METRIC_STATS if stats else METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
         "data": "synthetic",
         "config": {"workload": w.name, "B": B, "k": k, "sum_len": total,
-                   "offset_mode": mode, "page_size": args.page_size, "scores": "fp32",
+                   "offset_mode": mode, "page_size": args.page_size, "op": args.op, "scores": "fp32",
                    "l2": f"{n_copies} rotating input copies ({n_copies * in_bytes / 1e6:.0f} MB"
                          f" > 3x L2 {l2 / 1e6:.0f} MB): cold scores every step",
                    "timing": "CUDA events around graph replays of K launches on one stream",
@@ -422,12 +461,12 @@ def run_ours(args, rank, world, local):
         "achieved_gbs": achieved,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "peak_kind": peak_kind,
-                     "traffic": stored_traffic(w.name),
+                     "traffic": stored_traffic(w.name + (":stats" if stats else "")),
                      "algorithmic_bytes_per_launch": alg},
         "cpu_baseline": cpu,
         "e2e": {"value": whole_job_rate(B, e2e_ms, world), "unit": "rows/s",
                 "h2d_bytes_per_step": h_scores.numel() * 4 + 8 * B,
-                "d2h_bytes_per_step": B * k * 4, "ms_per_step": e2e_ms,
+                "d2h_bytes_per_step": B * out_cols * 4, "ms_per_step": e2e_ms,
                 "parity_vs_oracle": e2e_parity},
         "gpu_launches": args.steps * info["launches"],
         "clocks": clocks.summary(),
