@@ -237,6 +237,16 @@ __device__ __forceinline__ void mbar_wait_bounded(uint64_t *bar, uint32_t parity
         if (mbar_try_wait(bar, parity)) return;
 }
 
+// Programmatic dependent launch: the next grid in the stream may be staged
+// once every CTA of this one has started, and no CTA touches global memory
+// before the grids ahead of it in the stream have finished and their writes
+// are visible.
+__device__ __forceinline__ void grid_dependency_enter()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
 // ------------------------------------------------------------------------- //
 // Warp / block helpers.
 // ------------------------------------------------------------------------- //
@@ -961,6 +971,7 @@ __device__ RowGroup assign_rows(const Params &p, uint32_t crank, uint32_t csize,
 template <int THREADS>
 __global__ void __launch_bounds__(THREADS, 5) topk_row_kernel(const Params p)
 {
+    grid_dependency_enter();
     constexpr int NW = THREADS / 32;
     constexpr int U = 4;                       // quads in flight per lane
     constexpr uint32_t kZeroKey = 0x80000000u; // order key of +0.0
@@ -1940,6 +1951,7 @@ __device__ __forceinline__ void compact(bool staged, CCtrl &ctrl, const Slice &s
 template <int THREADS>
 __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kernel(const Params p)
 {
+    grid_dependency_enter();
     constexpr uint32_t kZeroKey = 0x80000000u;   // order key of +0.0
     constexpr uint32_t kZeroDigit = kZeroKey >> 21;
     constexpr uint32_t kChunk = 32768;           // bytes per bulk copy
@@ -2203,6 +2215,7 @@ __global__ void __launch_bounds__(THREADS) topk_stats_kernel(const float *scores
                                                              const int32_t *row_starts, const int32_t *lengths,
                                                              int32_t k, topk_row_stats *out)
 {
+    grid_dependency_enter();
     constexpr int BPT = kBins / THREADS;
     constexpr uint32_t kNone = 0xFFFFFFFFu;
     __shared__ uint32_t hist[kBins];
@@ -2635,14 +2648,17 @@ static int launch(const float *scores, int64_t n_scores, const int32_t *row_star
     cfg.blockDim = dim3((unsigned)pl.v->threads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)pl.smem;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (pl.v->cluster) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)pl.cluster;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
+        attr[1].id = cudaLaunchAttributeClusterDimension;
+        attr[1].val.clusterDim.x = (unsigned)pl.cluster;
+        attr[1].val.clusterDim.y = 1;
+        attr[1].val.clusterDim.z = 1;
+        cfg.numAttrs = 2;
     }
     if (cudaLaunchKernelEx(&cfg, pl.v->fn, prm) != cudaSuccess) {
         cudaGetLastError();
@@ -2696,6 +2712,11 @@ int topk_ragged_stats(const float *scores, int64_t n_scores, const int32_t *row_
     cfg.gridDim = dim3((unsigned)B, 1, 1);
     cfg.blockDim = dim3((unsigned)kStatsThreads, 1, 1);
     cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     if (cudaLaunchKernelEx(&cfg, topk_stats_kernel<kStatsThreads>, scores, n_scores, row_starts, lengths, k,
                            out) != cudaSuccess) {
         cudaGetLastError();
