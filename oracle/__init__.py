@@ -178,3 +178,41 @@ def row_stats(scores: np.ndarray, row_starts: np.ndarray, lengths: np.ndarray, k
             flags |= STAT_ZERO_BOUND
         out[i] = (L, n_zero, bb, tie, above, flags)
     return out, row_flags
+
+
+# --- the lightning-indexer scores that feed the selection ----------------------
+INDEXER_HEADS = 64
+INDEXER_DIM = 128
+
+
+def indexer_scores(q: np.ndarray, w: np.ndarray, bias, keys: np.ndarray, key_starts: np.ndarray,
+                   lengths: np.ndarray, score_starts: np.ndarray, n_scores: int, scale: float):
+    """The indexer scores of the DSA lightning indexer as the pages state
+    them (the decode batch of the vLLM / sglang pages' workloads: each
+    key t of row i scores s_t = sum over heads h of w[i, h] *
+    relu(scale * q[i, h] . k_t + b_i), with 64 heads of dimension 128; b_i is
+    an optional per-row logit shift, 0 for the plain indexer), in float64
+    from the given (bf16-valued) inputs.
+
+    Row i reads keys[key_starts[i] : key_starts[i] + L_i] and its scores go
+    to [score_starts[i], score_starts[i] + L_i) of an n_scores buffer.
+    Returns (scores float64[n_scores], written bool[n_scores]).  A row whose
+    windows leave [0, len(keys)) or [0, n_scores), or whose length is at
+    least 2^24, writes nothing.
+    """
+    q = np.asarray(q, dtype=np.float64).reshape(-1, INDEXER_HEADS, INDEXER_DIM)
+    w = np.asarray(w, dtype=np.float64).reshape(-1, INDEXER_HEADS)
+    keys = np.asarray(keys, dtype=np.float64).reshape(-1, INDEXER_DIM)
+    B = q.shape[0]
+    b = np.zeros(B) if bias is None else np.asarray(bias, dtype=np.float64).reshape(-1)
+    out = np.zeros(n_scores, dtype=np.float64)
+    written = np.zeros(n_scores, dtype=bool)
+    for i in range(B):
+        L = max(int(lengths[i]), 0)
+        ks, ss = int(key_starts[i]), int(score_starts[i])
+        if L == 0 or L >= MAX_LEN or ks < 0 or ks + L > keys.shape[0] or ss < 0 or ss + L > n_scores:
+            continue
+        logits = scale * (keys[ks:ks + L] @ q[i].T) + b[i]          # [L, H]
+        out[ss:ss + L] = np.maximum(logits, 0.0) @ w[i]
+        written[ss:ss + L] = True
+    return out, written
