@@ -1,7 +1,7 @@
 """Benchmark: deterministic exact ragged top-k on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--config NAME] [--impl ours|reference]
-                    [--page-size P] [--op topk|stats]
+                    [--page-size P] [--op topk|stats|indexer]
 
 A step is one call of the whole hot path (one launch of the library over one
 batch of rows).  The default workload is the decode batch: 64 rows with
@@ -12,7 +12,9 @@ from HBM.  Rank 0 prints one JSON line.
 
 --page-size P times the page-table transform (topk_ragged_paged) and
 --op stats the tie / plateau statistics op (topk_ragged_stats) on the same
-workload, in the same way.
+workload, in the same way.  --op indexer times the indexer + top-k chain
+(topk_ragged_indexer: the tensor-core indexer scores from bf16 queries and
+keys, then the selection) on the decode or prefill shape.
 
 --impl reference times the CPU oracle (the plain per-row sort the library is
 checked against) on the host cores, on a bounded sample of rows per step.
@@ -36,6 +38,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "ragged exact top-k rows/s and achieved HBM GB/s (k=2048) vs roofline"
 METRIC_STATS = "ragged tie/plateau statistics rows/s and achieved HBM GB/s (k=2048) vs roofline"
+METRIC_INDEXER = "lightning-indexer scores + exact top-k rows/s (k=2048) vs roofline"
 STATS_FIELDS = 6   # 32-bit fields of one topk_row_stats
 PEAKS_PATH = os.path.join(ROOT, "MEASURED_PEAKS.json")
 TRAFFIC_PATH = os.path.join(ROOT, "profiles", "traffic.json")
@@ -60,8 +63,9 @@ def parse_args():
     p.add_argument("--page-size", type=int, default=0,
                    help="write KV-cache slots through random per-row page tables of this "
                         "page size (topk_ragged_paged); 0: plain indices")
-    p.add_argument("--op", default="topk", choices=["topk", "stats"],
-                   help="topk: the selection; stats: per-row tie/plateau statistics")
+    p.add_argument("--op", default="topk", choices=["topk", "stats", "indexer"],
+                   help="topk: the selection; stats: per-row tie/plateau statistics; "
+                        "indexer: indexer scores on the tensor cores, then the selection")
     return p.parse_args()
 
 
@@ -100,8 +104,14 @@ def algorithmic_bytes_stats(total_len: int, B: int) -> int:
 
 
 def kernel_source_sha() -> str:
-    with open(KERNEL_SRC, "rb") as f:
-        return hashlib.sha256(f.read()).hexdigest()[:16]
+    """Hash of every kernel source file (csrc/*.cu, *.cuh, in name order)."""
+    h = hashlib.sha256()
+    csrc = os.path.dirname(KERNEL_SRC)
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh")):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode() + b"\0" + f.read())
+    return h.hexdigest()[:16]
 
 
 def stored_traffic(workload: str):
@@ -218,10 +228,51 @@ def time_oracle(w, seconds: float, rows_per_call=None, max_calls=None, op="topk"
     return rows / el, elems / el, threads, desc
 
 
+def run_reference_indexer(args):
+    import workloads as W
+    w = W.INDEXER[args.config](device="cpu")
+    ln = w.lengths.numpy()
+    t0 = time.perf_counter()
+    indexer_reference_sample(w, [0])
+    per_row = time.perf_counter() - t0
+    rows_per_step = max(1, min(w.B, int(120.0 / max(1, args.steps + args.warmup) / max(per_row, 1e-9))))
+    cursor = 0
+
+    def step():
+        nonlocal cursor
+        rows = [(cursor + j) % w.B for j in range(rows_per_step)]
+        cursor = (cursor + rows_per_step) % w.B
+        indexer_reference_sample(w, rows)
+        return int(ln[rows].sum())
+
+    for _ in range(args.warmup):
+        step()
+    elems = 0
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        elems += step()
+    el = time.perf_counter() - t0
+    value = rows_per_step * args.steps / el
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC_INDEXER, "value": value, "unit": "rows/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64 scores; u32 select",
+        "data": "synthetic", "config": {"workload": w.name, "B": w.B, "k": w.k, "op": "indexer",
+                                        "rows_per_step": rows_per_step},
+        "cpu_baseline": {"value": value, "unit": "rows/s", "cores": 1, "kind": "oracle",
+                         "sample": f"{rows_per_step} row(s) per step, rows cycled in order; {elems} keys "
+                                   f"in {el:.2f} s"},
+        "e2e": {"value": value, "unit": "rows/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
 def run_reference(args, rank):
     import workloads as W
 
     if rank != 0:
+        return
+    if args.op == "indexer":
+        run_reference_indexer(args)
         return
     w = W.make(args.config, device="cpu") if args.config in ("tiny", "adversarial") else None
     if w is None:
@@ -474,6 +525,219 @@ def run_ours(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+# --------------------------------------------------------------------------- #
+# The indexer + top-k chain.
+# --------------------------------------------------------------------------- #
+
+def indexer_bytes_flops(w) -> tuple[int, int]:
+    """Algorithmic bytes of the score kernel (every key row read once, the
+    queries, weights, shifts and metadata, the score writes) and its flops."""
+    B = w.B
+    nbytes = (256 * w.unique_key_rows() + 2 * 64 * 128 * B + 4 * 64 * B + 4 * B + 12 * B + 4 * w.n_scores)
+    return nbytes, 2 * 64 * 128 * w.n_scores
+
+
+def indexer_reference_sample(w, rows, bound=False):
+    """The oracle's indexer scores and selection for a list of rows; with
+    bound, also each score's error-bound magnitude (scale * sum_h w_h
+    sum_d |q_hd k_td| + sum_h w_h |x_h|), of which 2^-16 bounds the fp32 path."""
+    import numpy as np
+
+    import oracle
+    q = w.q[rows].float().cpu().numpy()
+    wt = w.w[rows].cpu().numpy()
+    b = w.bias[rows].cpu().numpy()
+    ln = w.lengths[rows].cpu().numpy()
+    ks = w.key_starts[rows].cpu().numpy()
+    lo, hi = int(ks.min()), int((ks + ln).max())
+    keys = w.keys[lo:hi].float().cpu().numpy()
+    ss = np.zeros(len(rows), dtype=np.int64)
+    ss[1:] = np.cumsum(ln)[:-1]
+    s, _ = oracle.indexer_scores(q, wt, b, keys, ks - lo, ln, ss, int(ln.sum()), w.scale)
+    oracle.topk_ragged(s.astype(np.float32), ss, ln, w.k, 0, with_values=False)
+    if not bound:
+        return s, ss
+    mag = np.zeros_like(s)
+    for j in range(len(rows)):
+        kj = keys[ks[j] - lo:ks[j] - lo + ln[j]].astype(np.float64)
+        x = w.scale * (kj @ q[j].astype(np.float64).T) + b[j]
+        mag[ss[j]:ss[j] + ln[j]] = (w.scale * (np.abs(kj) @ np.abs(q[j].astype(np.float64)).T) @ wt[j]
+                                    + np.abs(x) @ wt[j])
+    return s, ss, mag
+
+
+def run_indexer(args, rank, world, local):
+    import numpy as np
+    import torch
+
+    import oracle
+    import sparse_attention_deterministic_gb300 as pkg
+    import workloads as W
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    pkg.build()
+    pkg.init(device)
+    if args.config not in W.INDEXER:
+        raise SystemExit("--op indexer takes --config decode or prefill")
+    w = W.INDEXER[args.config](device=device)
+    B, k = w.B, w.k
+    scores = torch.zeros(w.n_scores, dtype=torch.float32, device=device)
+    out = torch.empty((B, k), dtype=torch.int32, device=device)
+    stream = torch.cuda.Stream(device)
+    args_t = (w.q, w.w, w.keys, w.key_starts, w.lengths, w.score_starts)
+
+    def chain(s=None):
+        pkg.topk_ragged_indexer(*args_t, k=k, bias=w.bias, scale=w.scale, scores=scores, out_idx=out, stream=s)
+
+    def scores_only(s=None):
+        pkg.indexer_scores(*args_t, bias=w.bias, scale=w.scale, out=scores, stream=s)
+
+    # Parity guard: the selection over the GPU's scores is the oracle's, and
+    # sampled rows' scores are within the fp32 bound of the oracle's float64.
+    with torch.cuda.stream(stream):
+        chain(stream)
+    stream.synchronize()
+    s_np = scores.cpu().numpy()
+    ln_np, ss_np = w.lengths.cpu().numpy(), w.score_starts.cpu().numpy()
+    ref_idx, _, _ = oracle.topk_ragged(s_np, ss_np, ln_np, k, 0, n_threads=len(os.sched_getaffinity(0)),
+                                       with_values=False)
+    parity = bool(np.array_equal(out.cpu().numpy(), ref_idx)) and pkg.device_status(device) == 0
+    sample = [0, B // 2, B - 1]
+    ref_s, ref_ss, mag = indexer_reference_sample(w, sample, bound=True)
+    worst = 0.0
+    for j, i in enumerate(sample):
+        L, a = int(ln_np[i]), int(ss_np[i])
+        got = s_np[a:a + L].astype(np.float64)
+        r0 = ref_ss[j]
+        err = np.abs(got - ref_s[r0:r0 + L]) / (2.0 ** -16 * mag[r0:r0 + L] + 1e-30)
+        worst = max(worst, float(err.max()))
+    scores_parity = worst <= 1.0
+
+    n_graph = 16
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=stream):
+        for _ in range(n_graph):
+            chain(torch.cuda.current_stream())
+    reps = max(1, args.steps // n_graph)
+    steps = reps * n_graph
+
+    def timed(fn_replay, n):
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        with torch.cuda.stream(stream):
+            ev0.record(stream)
+            for _ in range(n):
+                fn_replay()
+            ev1.record(stream)
+        ev1.synchronize()
+        return ev0.elapsed_time(ev1)
+
+    with ClockSampler(local) as clocks:
+        with torch.cuda.stream(stream):
+            for _ in range(args.warmup):
+                chain(stream)
+            g.replay()
+        stream.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        torch.cuda.synchronize(device)
+        ms = timed(g.replay, reps)
+        torch.cuda.synchronize(device)
+        if world > 1:
+            torch.distributed.barrier()
+        # the dominant kernel alone, same stream
+        with torch.cuda.stream(stream):
+            for _ in range(3):
+                scores_only(stream)
+        ms_scores = timed(lambda: scores_only(stream), n_graph * 4) / (n_graph * 4)
+    ms = max_over_ranks(ms, world)
+    ms_per_step = ms / steps
+    value = whole_job_rate(B, ms_per_step, world)
+
+    # End to end with host inputs: H2D of queries, weights, shifts, keys and
+    # metadata, the chain, D2H of the indices.
+    host = [t.cpu().pin_memory() for t in (w.q, w.w, w.bias, w.keys, w.key_starts, w.lengths, w.score_starts)]
+    dev_t = [torch.empty_like(t) for t in (w.q, w.w, w.bias, w.keys, w.key_starts, w.lengths, w.score_starts)]
+    h_out = torch.empty((B, k), dtype=torch.int32).pin_memory()
+
+    def e2e_step():
+        for d, h in zip(dev_t, host):
+            d.copy_(h, non_blocking=True)
+        pkg.topk_ragged_indexer(dev_t[0], dev_t[1], dev_t[3], dev_t[4], dev_t[5], dev_t[6], k=k, bias=dev_t[2],
+                                scale=w.scale, scores=scores, out_idx=out)
+        h_out.copy_(out, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        e2e_step()
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(args.e2e_steps):
+            e2e_step()
+        e1.record(stream)
+        e1.synchronize()
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.e2e_steps
+    e2e_parity = bool(np.array_equal(h_out.numpy(), ref_idx))
+
+    if rank != 0:
+        return
+    nbytes, flops = indexer_bytes_flops(w)
+    hbm, hbm_kind = hbm_peak()
+    bf16 = json.load(open(PEAKS_PATH)).get("bf16_tflops") if os.path.exists(PEAKS_PATH) else None
+    bf16_kind = "measured" if bf16 else "fallback"
+    bf16 = bf16 or 1900.0
+    t_hbm, t_tensor = nbytes / (hbm * 1e9), flops / (bf16 * 1e12)
+    if t_hbm >= t_tensor:
+        achieved = nbytes / (ms_scores * 1e-3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "peak_kind": hbm_kind, "algorithmic_bytes_per_launch": nbytes}
+    else:
+        achieved = flops / (ms_scores * 1e-3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": bf16, "unit": "TFLOP/s",
+                "frac": achieved / bf16, "peak_kind": bf16_kind + " (dense bf16, burst)",
+                "algorithmic_flops_per_launch": flops}
+    roof.update({"kernel": "indexer_scores_kernel", "kernel_ms": ms_scores,
+                 "traffic": stored_traffic(w.name)})
+    cpu = None
+    if not args.no_cpu_baseline and world == 1:
+        t0 = time.perf_counter()
+        rows_done = elems = 0
+        i = 0
+        while time.perf_counter() - t0 < args.cpu_seconds:
+            indexer_reference_sample(w, [i % B])
+            rows_done += 1
+            elems += int(ln_np[i % B])
+            i += 1
+        el = time.perf_counter() - t0
+        cpu = {"value": rows_done / el, "unit": "rows/s", "cores": 1, "kind": "oracle",
+               "sample": f"{rows_done} row(s) of the {w.name} workload, one per oracle call (float64 scores, "
+                         f"then the selection): {elems} keys in {el:.2f} s"}
+    line = {
+        "metric": METRIC_INDEXER, "value": value, "unit": "rows/s", "n_gpus": world,
+        "steps": steps, "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16 x bf16 -> f32; u32 select", "data": "synthetic",
+        "config": {"workload": w.name, "B": B, "k": k, "sum_len": w.n_scores, "key_rows": w.unique_key_rows(),
+                   "op": "indexer", "l2": f"keys {w.keys.numel() * 2 / 1e6:.0f} MB, queries "
+                                         f"{w.q.numel() * 2 / 1e6:.0f} MB: inputs larger than L2"
+                                         if w.keys.numel() * 2 > 3 * 129e6 else
+                                         "keys shared by every row stay in L2; queries stream",
+                   "timing": "CUDA events around graph replays of 16 chained calls on one stream",
+                   "parity_vs_oracle": parity, "scores_within_bound": scores_parity,
+                   "scores_worst_err_over_bound": worst},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": whole_job_rate(B, e2e_ms, world), "unit": "rows/s",
+                "h2d_bytes_per_step": sum(h.numel() * h.element_size() for h in host),
+                "d2h_bytes_per_step": B * k * 4, "ms_per_step": e2e_ms, "parity_vs_oracle": e2e_parity},
+        "gpu_launches": 2 * steps,
+        "clocks": clocks.summary(),
+    }
+    print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse_args()
     if args.warmup < 3:
@@ -481,6 +745,9 @@ def main():
     rank, world, local = dist_env()
     if args.impl == "reference":
         run_reference(args, rank)
+        return
+    if args.op == "indexer":
+        run_indexer(args, rank, world, local)
         return
     run_ours(args, rank, world, local)
 

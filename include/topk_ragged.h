@@ -32,7 +32,7 @@
 extern "C" {
 #endif
 
-#define TOPK_RAGGED_ABI_VERSION 3
+#define TOPK_RAGGED_ABI_VERSION 4
 #define TOPK_RAGGED_MAX_K 4096
 /* Row lengths must stay below 2^24, the envelope of the 24-bit index field. */
 #define TOPK_RAGGED_MAX_LEN (1 << 24)
@@ -178,6 +178,52 @@ enum {
 int topk_ragged_stats(const float *scores, int64_t n_scores, const int32_t *row_starts,
                       const int32_t *lengths, int32_t B, int32_t k, topk_row_stats *out,
                       void *stream);
+
+/*
+ * Lightning-indexer scores on the tensor cores (tcgen05 MMAs fed by TMA):
+ * key t of row i scores
+ *     s_t = sum over h < 64 of w[i][h] * relu(scale * (q[i][h] . k_t) + bias[i])
+ * with 64 heads of dimension 128, the indexer of the vLLM and sglang pages'
+ * decode and prefill workloads (bias is an optional per-row logit shift).
+ * Products and sums run in fp32 on the tensor cores; the epilogue sums the
+ * heads in index order with fused multiply-adds, so a call is deterministic.
+ *
+ * q             device, bf16 bit patterns, [B][64][128], 16-byte aligned.
+ * w             device fp32 [B][64], 16-byte aligned.
+ * bias          device fp32 [B], or NULL for 0.
+ * keys          device, bf16 bit patterns, [n_keys][128], 16-byte aligned;
+ *               1 <= n_keys < 2^31.
+ * key_starts, lengths, score_starts
+ *               device int32 [B]: row i reads keys[key_starts[i] + j] and
+ *               writes scores[score_starts[i] + j] for j < L_i (a negative
+ *               length reads as 0).  Rows may share keys (a causal prefill
+ *               chunk) and must not share score windows.
+ * scores        device fp32 [n_scores], caller-owned; only the rows' score
+ *               windows are written.
+ * A row whose key or score window leaves its buffer, or with L_i >= 2^24,
+ * writes nothing and sets its TOPK_DEV_* bit.  Inputs must be finite (a NaN
+ * logit reads as 0 through the relu).  One launch, stream-ordered, no
+ * allocation, capturable after topk_ragged_init.  Returns TOPK_OK,
+ * TOPK_ERR_INVALID_ARG (B < 0, B * 64 >= 2^31, n_keys or n_scores out of
+ * range, a non-finite scale, NULL or misaligned pointers),
+ * TOPK_ERR_NOT_INITIALIZED, TOPK_ERR_UNSUPPORTED_DEVICE or TOPK_ERR_CUDA.
+ */
+int topk_ragged_indexer_scores(const uint16_t *q, const float *w, const float *bias, const uint16_t *keys,
+                               int64_t n_keys, const int32_t *key_starts, const int32_t *lengths,
+                               const int32_t *score_starts, int32_t B, float scale, float *scores,
+                               int64_t n_scores, void *stream);
+
+/*
+ * The indexer scores into the caller's `scores` buffer, then topk_ragged over
+ * them (row i's window: score_starts[i], L_i): two launches on `stream`.
+ * Indices are row-local (j, the key's place in the row's key window);
+ * flags is 0 or TOPK_EXCLUDE_NEG_INF.  Arguments and errors as for the two
+ * calls.
+ */
+int topk_ragged_indexer(const uint16_t *q, const float *w, const float *bias, const uint16_t *keys,
+                        int64_t n_keys, const int32_t *key_starts, const int32_t *lengths,
+                        const int32_t *score_starts, int32_t B, float scale, float *scores, int64_t n_scores,
+                        int32_t k, int32_t flags, int32_t *out_idx, float *out_val, void *stream);
 
 /*
  * Reads the current device's status word (an OR of TOPK_DEV_* bits from all

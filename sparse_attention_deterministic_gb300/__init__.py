@@ -11,13 +11,14 @@ from ._native import EXPORTS, LIB_PATH, TopkError, build, lib, strerror
 from .binding import (MAX_K, MAX_LEN, PAD_VALUE_BITS, ROW_STATS_FIELDS, TOPK_DEV_BAD_WINDOW,
                       TOPK_DEV_INTERNAL, TOPK_DEV_LEN_ENVELOPE, TOPK_OFFSET_ROW_LOCAL,
                       TOPK_EXCLUDE_NEG_INF, TOPK_OFFSET_ROW_START, TOPK_STAT_HAS_BOUNDARY,
-                      TOPK_STAT_STRADDLE, TOPK_STAT_ZERO_BOUND, device_status, init, launch_info,
-                      topk_ragged, topk_ragged_stats)
+                      TOPK_STAT_STRADDLE, TOPK_STAT_ZERO_BOUND, INDEXER_DIM, INDEXER_HEADS, device_status,
+                      indexer_scores, init, launch_info, topk_ragged, topk_ragged_indexer, topk_ragged_stats)
 
 __all__ = [
     "EXPORTS", "LIB_PATH", "TopkError", "build", "lib", "strerror", "MAX_K", "MAX_LEN",
     "PAD_VALUE_BITS", "TOPK_DEV_BAD_WINDOW", "TOPK_DEV_INTERNAL", "TOPK_DEV_LEN_ENVELOPE",
     "TOPK_OFFSET_ROW_LOCAL", "TOPK_OFFSET_ROW_START", "TOPK_EXCLUDE_NEG_INF", "device_status", "init",
     "launch_info", "ROW_STATS_FIELDS", "TOPK_STAT_HAS_BOUNDARY", "TOPK_STAT_STRADDLE",
-    "TOPK_STAT_ZERO_BOUND", "topk_ragged", "topk_ragged_stats",
+    "TOPK_STAT_ZERO_BOUND", "topk_ragged", "topk_ragged_stats", "INDEXER_HEADS", "INDEXER_DIM",
+    "indexer_scores", "topk_ragged_indexer",
 ]

@@ -27,6 +27,8 @@ EXPORTS = (
     "topk_ragged",
     "topk_ragged_paged",
     "topk_ragged_stats",
+    "topk_ragged_indexer_scores",
+    "topk_ragged_indexer",
     "topk_ragged_device_status",
     "topk_ragged_launch_info",
 )
@@ -45,7 +47,9 @@ def nvcc() -> str:
 def build(force: bool = False, verbose: bool = False) -> str:
     """Compile the CUDA library in-tree; returns its path."""
     os.makedirs(BUILD_DIR, exist_ok=True)
-    newest = max(os.path.getmtime(SRC), os.path.getmtime(HEADER))
+    csrc = os.path.dirname(SRC)
+    newest = max([os.path.getmtime(HEADER)] + [os.path.getmtime(os.path.join(csrc, f))
+                                                for f in os.listdir(csrc) if f.endswith((".cu", ".cuh"))])
     if not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= newest:
         return LIB_PATH
     tmp = f"{LIB_PATH}.tmp{os.getpid()}"
@@ -100,6 +104,11 @@ def lib() -> ctypes.CDLL:
         so.topk_ragged_stats.argtypes = [ctypes.c_void_p, ctypes.c_int64, ctypes.c_void_p, ctypes.c_void_p,
                                          ctypes.c_int32, ctypes.c_int32, ctypes.c_void_p, ctypes.c_void_p]
         so.topk_ragged_stats.restype = ctypes.c_int
+        vp, i32, i64, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float
+        so.topk_ragged_indexer_scores.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, i32, f32, vp, i64, vp]
+        so.topk_ragged_indexer_scores.restype = ctypes.c_int
+        so.topk_ragged_indexer.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, i32, f32, vp, i64, i32, i32, vp, vp, vp]
+        so.topk_ragged_indexer.restype = ctypes.c_int
         so.topk_ragged_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_void_p]
         so.topk_ragged_device_status.restype = ctypes.c_int
         so.topk_ragged_launch_info.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,

@@ -146,6 +146,101 @@ def topk_ragged_stats(scores: torch.Tensor, row_starts: torch.Tensor, lengths: t
     return out
 
 
+INDEXER_HEADS = 64
+INDEXER_DIM = 128
+
+
+def _indexer_args(q, w, keys, key_starts, lengths, score_starts, bias, scale):
+    _check(q, "q", torch.bfloat16)
+    dev = q.device
+    _check(w, "w", torch.float32, dev)
+    _check(keys, "keys", torch.bfloat16, dev)
+    for t, name in ((key_starts, "key_starts"), (lengths, "lengths"), (score_starts, "score_starts")):
+        _check(t, name, torch.int32, dev)
+    B = key_starts.numel()
+    if q.numel() != B * INDEXER_HEADS * INDEXER_DIM or w.numel() != B * INDEXER_HEADS:
+        raise ValueError(f"q must be [B, {INDEXER_HEADS}, {INDEXER_DIM}] and w [B, {INDEXER_HEADS}]")
+    if lengths.numel() != B or score_starts.numel() != B:
+        raise ValueError("key_starts, lengths and score_starts differ in size")
+    if keys.numel() % INDEXER_DIM:
+        raise ValueError(f"keys must be [n_keys, {INDEXER_DIM}]")
+    if bias is not None:
+        _check(bias, "bias", torch.float32, dev)
+        if bias.numel() != B:
+            raise ValueError("bias must hold B entries")
+    scale = 1.0 / INDEXER_DIM ** 0.5 if scale is None else float(scale)
+    return dev, B, scale
+
+
+def indexer_scores(q: torch.Tensor, w: torch.Tensor, keys: torch.Tensor, key_starts: torch.Tensor,
+                   lengths: torch.Tensor, score_starts: torch.Tensor, n_scores: int | None = None,
+                   scale: float | None = None, bias: torch.Tensor | None = None,
+                   out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Lightning-indexer scores on the tensor cores (topk_ragged_indexer_scores).
+
+    q bf16 [B, 64, 128], w fp32 [B, 64], keys bf16 [n_keys, 128], bias fp32
+    [B] or None, key_starts / lengths / score_starts int32 [B]; scale defaults
+    to 1/sqrt(128).  Writes row i's scores to out[score_starts[i] + j] and
+    returns out (fp32 [n_scores], allocated with zeros when not given).
+    """
+    dev, B, scale = _indexer_args(q, w, keys, key_starts, lengths, score_starts, bias, scale)
+    if out is None:
+        if n_scores is None:
+            raise ValueError("give n_scores or out")
+        out = torch.zeros(int(n_scores), dtype=torch.float32, device=dev)
+    else:
+        _check(out, "out", torch.float32, dev)
+    with torch.cuda.device(dev):
+        rc = lib().topk_ragged_indexer_scores(
+            q.data_ptr() if B else None, w.data_ptr() if B else None,
+            bias.data_ptr() if (bias is not None and B) else None, keys.data_ptr() if keys.numel() else None,
+            keys.numel() // INDEXER_DIM, key_starts.data_ptr() if B else None, lengths.data_ptr() if B else None,
+            score_starts.data_ptr() if B else None, B, scale, out.data_ptr() if out.numel() else None,
+            out.numel(), _stream_handle(dev, stream))
+    if rc != 0:
+        raise TopkError(rc, "topk_ragged_indexer_scores")
+    return out
+
+
+def topk_ragged_indexer(q: torch.Tensor, w: torch.Tensor, keys: torch.Tensor, key_starts: torch.Tensor,
+                        lengths: torch.Tensor, score_starts: torch.Tensor, k: int = 2048, flags: int = 0,
+                        scale: float | None = None, bias: torch.Tensor | None = None,
+                        scores: torch.Tensor | None = None, n_scores: int | None = None,
+                        out_idx: torch.Tensor | None = None, out_val: torch.Tensor | None = None,
+                        with_values: bool = False, stream=None):
+    """Indexer scores, then the deterministic top-k over them
+    (topk_ragged_indexer).  `scores` is the caller's scratch (allocated when
+    not given).  Returns (out_idx, out_val or None, scores)."""
+    dev, B, scale = _indexer_args(q, w, keys, key_starts, lengths, score_starts, bias, scale)
+    if scores is None:
+        if n_scores is None:
+            raise ValueError("give n_scores or scores")
+        scores = torch.zeros(int(n_scores), dtype=torch.float32, device=dev)
+    else:
+        _check(scores, "scores", torch.float32, dev)
+    if out_idx is None:
+        out_idx = torch.empty((B, k), dtype=torch.int32, device=dev)
+    else:
+        _check(out_idx, "out_idx", torch.int32, dev)
+        if out_idx.numel() != B * k:
+            raise ValueError("out_idx must hold B * k entries")
+    if out_val is None and with_values:
+        out_val = torch.empty((B, k), dtype=torch.float32, device=dev)
+    elif out_val is not None:
+        _check(out_val, "out_val", torch.float32, dev)
+    with torch.cuda.device(dev):
+        rc = lib().topk_ragged_indexer(
+            q.data_ptr() if B else None, w.data_ptr() if B else None,
+            bias.data_ptr() if (bias is not None and B) else None, keys.data_ptr() if keys.numel() else None,
+            keys.numel() // INDEXER_DIM, key_starts.data_ptr() if B else None, lengths.data_ptr() if B else None,
+            score_starts.data_ptr() if B else None, B, scale, scores.data_ptr() if scores.numel() else None,
+            scores.numel(), int(k), int(flags), out_idx.data_ptr() if B else None,
+            out_val.data_ptr() if (out_val is not None and B) else None, _stream_handle(dev, stream))
+    if rc != 0:
+        raise TopkError(rc, "topk_ragged_indexer")
+    return out_idx, out_val, scores
+
+
 def device_status(device=None, stream=None) -> int:
     """Read and clear the device status word (synchronises the stream)."""
     dev = torch.device("cuda", torch.cuda.current_device() if device is None else

@@ -31,6 +31,8 @@
 // Nothing is allocated; the only global state is a status word for data
 // errors.  All cross-CTA synchronisation uses hardware cluster barriers.
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -2352,6 +2354,8 @@ __global__ void __launch_bounds__(THREADS) topk_stats_kernel(const float *scores
     }
 }
 
+#include "indexer_scores.cuh"
+
 // ------------------------------------------------------------------------- //
 // Host side.
 // ------------------------------------------------------------------------- //
@@ -2380,6 +2384,20 @@ struct DeviceInfo {
 };
 
 std::mutex g_mutex;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode_tiled = nullptr;   // the driver's TMA descriptor encoder
+
+// A TMA map over rows of 128 bf16 (256 bytes each): boxes of 64 columns
+// (128 bytes, the 128-byte swizzle span) by box_rows rows.
+bool encode_bf16_rows(CUtensorMap *map, const void *base, uint64_t rows, uint32_t box_rows)
+{
+    const cuuint64_t dims[2] = {(cuuint64_t)kIxDim, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)kIxDim * 2};
+    const cuuint32_t box[2] = {64, box_rows};
+    const cuuint32_t elem[2] = {1, 1};
+    return g_encode_tiled(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims, strides, box,
+                          elem, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 DeviceInfo g_devices[kMaxDevices];
 
 struct Plan {
@@ -2507,6 +2525,20 @@ int init_locked(int device)
         if (v.cluster && cudaFuncSetAttribute((const void *)v.fn,
                                               cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
             rc = TOPK_ERR_CUDA;
+    }
+    if (rc == TOPK_OK && cudaFuncSetAttribute((const void *)indexer_scores_kernel<kIxThreads>,
+                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                              (int)kIxSmemBytes) != cudaSuccess)
+        rc = TOPK_ERR_CUDA;
+    if (rc == TOPK_OK && !g_encode_tiled) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) !=
+                cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || !fn)
+            rc = TOPK_ERR_CUDA;
+        else
+            g_encode_tiled = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
     }
     // Which cluster sizes each clustered variant can actually co-schedule
     // with the shared memory the planner gives it.
@@ -2723,6 +2755,74 @@ int topk_ragged_stats(const float *scores, int64_t n_scores, const int32_t *row_
         return TOPK_ERR_CUDA;
     }
     return TOPK_OK;
+}
+
+int topk_ragged_indexer_scores(const uint16_t *q, const float *w, const float *bias, const uint16_t *keys,
+                               int64_t n_keys, const int32_t *key_starts, const int32_t *lengths,
+                               const int32_t *score_starts, int32_t B, float scale, float *scores, int64_t n_scores,
+                               void *stream)
+{
+    if (B < 0 || n_keys < 1 || n_keys >= ((int64_t)1 << 31) || n_scores < 0 || n_scores >= ((int64_t)1 << 31))
+        return TOPK_ERR_INVALID_ARG;
+    if ((int64_t)B * kIxHeads >= ((int64_t)1 << 31) || !(scale == scale) || scale > 3.0e38f || scale < -3.0e38f)
+        return TOPK_ERR_INVALID_ARG;
+    if (B == 0) return TOPK_OK;
+    if (!q || !w || !keys || !key_starts || !lengths || !score_starts || (!scores && n_scores > 0))
+        return TOPK_ERR_INVALID_ARG;
+    if (((uintptr_t)q & 15u) || ((uintptr_t)keys & 15u) || ((uintptr_t)w & 15u) || ((uintptr_t)bias & 3u) ||
+        ((uintptr_t)scores & 3u))
+        return TOPK_ERR_INVALID_ARG;
+    cudaStream_t st = (cudaStream_t)stream;
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return TOPK_ERR_CUDA;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return TOPK_ERR_CUDA;
+    const int rc = ensure_init(device, cap == cudaStreamCaptureStatusNone);
+    if (rc != TOPK_OK) return rc;
+    CUtensorMap tmap_k, tmap_q;
+    if (!encode_bf16_rows(&tmap_k, keys, (uint64_t)n_keys, kIxTile) ||
+        !encode_bf16_rows(&tmap_q, q, (uint64_t)B * kIxHeads, kIxHeads))
+        return TOPK_ERR_INVALID_ARG;
+    IxParams prm;
+    prm.w = w;
+    prm.bias = bias;
+    prm.key_starts = key_starts;
+    prm.lengths = lengths;
+    prm.score_starts = score_starts;
+    prm.scores = scores;
+    prm.n_keys = n_keys;
+    prm.n_scores = n_scores;
+    prm.B = B;
+    prm.scale = scale;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)g_devices[device].sm_count, 1, 1);
+    cfg.blockDim = dim3((unsigned)kIxThreads, 1, 1);
+    cfg.dynamicSmemBytes = kIxSmemBytes;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaLaunchKernelEx(&cfg, indexer_scores_kernel<kIxThreads>, tmap_k, tmap_q, prm) != cudaSuccess) {
+        cudaGetLastError();
+        return TOPK_ERR_CUDA;
+    }
+    return TOPK_OK;
+}
+
+int topk_ragged_indexer(const uint16_t *q, const float *w, const float *bias, const uint16_t *keys, int64_t n_keys,
+                        const int32_t *key_starts, const int32_t *lengths, const int32_t *score_starts, int32_t B,
+                        float scale, float *scores, int64_t n_scores, int32_t k, int32_t flags, int32_t *out_idx,
+                        float *out_val, void *stream)
+{
+    if ((flags & ~TOPK_EXCLUDE_NEG_INF) != 0) return TOPK_ERR_INVALID_ARG;
+    int rc = validate(scores, n_scores, score_starts, lengths, B, k, flags, out_idx);
+    if (rc != TOPK_OK || B == 0) return rc;
+    rc = topk_ragged_indexer_scores(q, w, bias, keys, n_keys, key_starts, lengths, score_starts, B, scale, scores,
+                                    n_scores, stream);
+    if (rc != TOPK_OK) return rc;
+    return topk_ragged(scores, n_scores, score_starts, lengths, B, k, flags, out_idx, out_val, stream);
 }
 
 int topk_ragged_device_status(uint32_t *host_out, void *stream)

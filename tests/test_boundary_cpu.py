@@ -39,7 +39,7 @@ def test_exports_every_declared_symbol(so):
 
 
 def test_abi_version_and_strerror(so):
-    assert so.topk_ragged_abi_version() == 3
+    assert so.topk_ragged_abi_version() == 4
     for st in range(5):
         assert pkg.strerror(st)
     assert pkg.strerror(99) == "unknown status"

@@ -1,0 +1,188 @@
+"""The lightning-indexer scores on the tensor cores (topk_ragged_indexer_scores)
+against the oracle's float64 scores, and the indexer + top-k chain
+(topk_ragged_indexer) against the oracle's selection over the GPU's own scores.
+
+Tolerance.  The inputs are bf16, so every product q_hd * k_td is exact in
+fp32; the tensor cores sum 128 of them per head in fp32, and the epilogue
+applies scale and bias (one fused multiply-add), the relu and a 64-term
+fused multiply-add chain over heads.  With u = 2^-24 per rounding, the error
+is at most about 128 * 2u * scale * sum_h w_h sum_d |q_hd k_td| (allowing the
+tensor-core adds one extra bit) plus about 66 u * sum_h w_h |x_h| for the
+epilogue, x_h the head logit.  2^-16 times the sum of those two magnitudes
+bounds both with room to spare; it is the bar below, per element.
+
+The selection is decided in fp32 on both sides: the oracle's top-k runs over
+the GPU's scores, so the indices must agree bit for bit.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import sparse_attention_deterministic_gb300 as pkg
+
+pytestmark = pytest.mark.gpu
+H, D = 64, 128
+SENTINEL = -7.25
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    pkg.build()
+    pkg.init()
+
+
+def make_case(lengths, shared_keys=False, seed=0, bias=True, rho=0.99, gap=0):
+    """Correlated-head queries (as the workloads' indexer), U(0,1) head
+    weights, N(0,1) bf16 keys; decode layout (own keys per row) or a causal
+    prefill layout (every row reads the first L_i keys)."""
+    g = torch.Generator().manual_seed(seed)
+    B = len(lengths)
+    lengths = torch.tensor(lengths, dtype=torch.int32)
+    qbar = torch.randn(B, 1, D, generator=g)
+    q = (rho ** 0.5 * qbar + (1 - rho) ** 0.5 * torch.randn(B, H, D, generator=g)).to(torch.bfloat16)
+    w = torch.rand(B, H, generator=g)
+    b = (-0.6 * torch.rand(B, generator=g)) if bias else None
+    if shared_keys:
+        n_keys = max(1, int(lengths.max()))
+        key_starts = torch.zeros(B, dtype=torch.int32)
+    else:
+        key_starts = torch.zeros(B, dtype=torch.int32)
+        key_starts[1:] = torch.cumsum(lengths + gap, 0)[:-1].to(torch.int32)
+        n_keys = max(1, int((lengths + gap).sum()))
+    keys = torch.randn(n_keys, D, generator=g).to(torch.bfloat16)
+    score_starts = torch.zeros(B, dtype=torch.int32)
+    score_starts[1:] = torch.cumsum(lengths + 3, 0)[:-1].to(torch.int32)
+    n_scores = int((lengths + 3).sum())
+    return dict(q=q, w=w, bias=b, keys=keys, key_starts=key_starts, lengths=lengths,
+                score_starts=score_starts, n_scores=n_scores)
+
+
+def gpu_scores(c, scale=None):
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in c.items()}
+    out = torch.full((c["n_scores"],), SENTINEL, dtype=torch.float32, device="cuda")
+    pkg.indexer_scores(d["q"], d["w"], d["keys"], d["key_starts"], d["lengths"], d["score_starts"],
+                       scale=scale, bias=d["bias"], out=out)
+    torch.cuda.synchronize()
+    return out.cpu().numpy()
+
+
+def oracle_scores(c, scale):
+    q = c["q"].float().numpy()
+    keys = c["keys"].float().numpy()
+    s, written = oracle.indexer_scores(q, c["w"].numpy(), None if c["bias"] is None else c["bias"].numpy(),
+                                       keys, c["key_starts"].numpy(), c["lengths"].numpy(),
+                                       c["score_starts"].numpy(), c["n_scores"], scale)
+    # the error bound's magnitudes, per written score
+    mag = np.zeros(c["n_scores"])
+    qa, w = np.abs(q.astype(np.float64)), c["w"].numpy().astype(np.float64)
+    b = np.zeros(len(c["lengths"])) if c["bias"] is None else c["bias"].numpy().astype(np.float64)
+    for i in range(len(c["lengths"])):
+        L, ks, ss = int(c["lengths"][i]), int(c["key_starts"][i]), int(c["score_starts"][i])
+        if L <= 0 or not written[ss:ss + L].all():
+            continue
+        k64 = keys[ks:ks + L].astype(np.float64)
+        x = scale * (k64 @ q[i].astype(np.float64).T) + b[i]
+        mag[ss:ss + L] = scale * ((np.abs(k64) @ qa[i].T) @ w[i]) + np.abs(x) @ w[i]
+    return s, written, mag
+
+
+def assert_scores(c, scale=None):
+    scale = 1.0 / D ** 0.5 if scale is None else scale
+    got = gpu_scores(c, scale)
+    want, written, mag = oracle_scores(c, scale)
+    assert (got[~written] == SENTINEL).all(), "a score outside the rows' windows was written"
+    err = np.abs(got[written].astype(np.float64) - want[written])
+    tol = 2.0 ** -16 * mag[written] + 1e-30
+    bad = np.flatnonzero(err > tol)
+    assert bad.size == 0, (f"{bad.size} scores out of tolerance; worst ratio "
+                           f"{(err / tol).max():.3g}, first at {np.flatnonzero(written)[bad[0]]}")
+    return got
+
+
+def test_single_tile_single_row():
+    assert_scores(make_case([128], bias=False))
+
+
+@pytest.mark.parametrize("L", [1, 2, 127, 129, 255, 256, 1000])
+def test_partial_tiles(L):
+    assert_scores(make_case([L], seed=L))
+
+
+def test_rows_mixed_lengths_and_empty():
+    assert_scores(make_case([0, 5, 300, 0, 128, 4097, 1, 700], seed=3, gap=7))
+
+
+def test_shared_keys_causal_prefill_layout():
+    lengths = [max(1, (i + 1) // 4) for i in range(600)]
+    assert_scores(make_case(lengths, shared_keys=True, seed=4))
+
+
+def test_decode_layout_many_rows():
+    g = torch.Generator().manual_seed(5)
+    lengths = torch.randint(1, 20000, (64,), generator=g).tolist()
+    assert_scores(make_case(lengths, seed=5))
+
+
+@pytest.mark.parametrize("scale", [1.0, 0.01])
+def test_other_scales(scale):
+    assert_scores(make_case([3000, 17], seed=6), scale=scale)
+
+
+def test_repeatable_and_rejected_rows():
+    c = make_case([200, 300, 50], seed=7)
+    pkg.device_status()   # clear what earlier calls left
+    a = gpu_scores(c)
+    assert np.array_equal(a, gpu_scores(c))
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in c.items()}
+    bad_starts = d["key_starts"].clone()
+    bad_starts[1] = int(d["keys"].shape[0]) - 10          # key window leaves the buffer
+    out = torch.full((c["n_scores"],), SENTINEL, device="cuda")
+    pkg.indexer_scores(d["q"], d["w"], d["keys"], bad_starts, d["lengths"], d["score_starts"],
+                       bias=d["bias"], out=out)
+    torch.cuda.synchronize()
+    got = out.cpu().numpy()
+    assert pkg.device_status() == pkg.TOPK_DEV_BAD_WINDOW
+    ss = c["score_starts"].numpy()
+    assert (got[ss[1]:ss[1] + 300] == SENTINEL).all()
+    assert np.array_equal(got[ss[0]:ss[0] + 200], a[ss[0]:ss[0] + 200])
+
+
+@pytest.mark.parametrize("k", [1, 2048, 4096])
+def test_indexer_then_topk_equals_oracle_selection(k):
+    g = torch.Generator().manual_seed(8)
+    c = make_case(torch.randint(1, 30000, (40,), generator=g).tolist(), seed=8)
+    d = {kk: (v.cuda() if isinstance(v, torch.Tensor) else v) for kk, v in c.items()}
+    idx, val, scores = pkg.topk_ragged_indexer(d["q"], d["w"], d["keys"], d["key_starts"], d["lengths"],
+                                               d["score_starts"], k=k, bias=d["bias"], n_scores=c["n_scores"],
+                                               with_values=True)
+    torch.cuda.synchronize()
+    s = scores.cpu().numpy()
+    ref_idx, ref_val, _ = oracle.topk_ragged(s, c["score_starts"].numpy(), c["lengths"].numpy(), k, 0)
+    assert np.array_equal(idx.cpu().numpy(), ref_idx)
+    assert np.array_equal(val.cpu().numpy().view(np.uint32), ref_val.view(np.uint32))
+    # the chain's scores are the standalone op's
+    alone = gpu_scores(c)
+    for i in range(len(c["lengths"])):
+        a, L = int(c["score_starts"][i]), int(c["lengths"][i])
+        assert np.array_equal(s[a:a + L], alone[a:a + L])
+
+
+def test_graph_capture_of_the_chain():
+    c = make_case([5000, 70000, 1234], seed=9)
+    d = {kk: (v.cuda() if isinstance(v, torch.Tensor) else v) for kk, v in c.items()}
+    scores = torch.zeros(c["n_scores"], device="cuda")
+    idx = torch.empty((3, 2048), dtype=torch.int32, device="cuda")
+    args = (d["q"], d["w"], d["keys"], d["key_starts"], d["lengths"], d["score_starts"])
+    ref, _, _ = pkg.topk_ragged_indexer(*args, bias=d["bias"], scores=scores.clone())
+    st = torch.cuda.Stream()
+    with torch.cuda.stream(st):
+        pkg.topk_ragged_indexer(*args, bias=d["bias"], scores=scores, out_idx=idx)
+    torch.cuda.synchronize()
+    idx.zero_()
+    gr = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(gr, stream=st):
+        pkg.topk_ragged_indexer(*args, bias=d["bias"], scores=scores, out_idx=idx)
+    gr.replay()
+    torch.cuda.synchronize()
+    assert torch.equal(idx, ref)

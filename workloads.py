@@ -340,3 +340,72 @@ def random_bits(B: int, L: int, k: int, seed: int = 19, alphabet=None) -> Worklo
         bits = a[torch.randint(0, len(alphabet), (B, L), generator=g)]
     bits = (bits - ((bits >> 31) << 32)).to(torch.int32)
     return _uniform("random_bits", bits.view(torch.float32), k)
+
+
+# --------------------------------------------------------------------------- #
+# Indexer inputs: the queries, head weights and keys the decode and prefill
+# scores are made from, for the indexer + top-k chain.
+# --------------------------------------------------------------------------- #
+
+@dataclasses.dataclass
+class IndexerWorkload:
+    name: str
+    q: torch.Tensor             # bf16 [B, 64, 128]
+    w: torch.Tensor             # fp32 [B, 64]
+    bias: torch.Tensor          # fp32 [B]: the per-row logit shift mu
+    keys: torch.Tensor          # bf16 [n_keys, 128]
+    key_starts: torch.Tensor    # int32 [B]
+    lengths: torch.Tensor       # int32 [B]
+    score_starts: torch.Tensor  # int32 [B]
+    n_scores: int
+    k: int
+    scale: float = 1.0 / math.sqrt(HEAD_DIM)
+
+    @property
+    def B(self) -> int:
+        return int(self.lengths.numel())
+
+    def unique_key_rows(self) -> int:
+        return int(self.keys.shape[0])
+
+
+def decode_indexer(device="cpu", B: int = 64, lmin: int = 4096, lmax: int = 131072,
+                   k: int = 2048) -> IndexerWorkload:
+    """The decode batch's shape as indexer inputs: B rows, lengths ~
+    U{lmin..lmax} (the decode workload's lengths), each row its own block of
+    N(0,1) bf16 keys, correlated-head bf16 queries, w ~ U(0,1), mu ~
+    U(-0.6, 0); keys and scores laid out contiguously."""
+    g = _gen(seed_of("decode"), device)
+    lengths = torch.randint(lmin, lmax + 1, (B,), generator=g, device=device).to(torch.int32)
+    starts = _contiguous_starts(lengths)
+    total = int(lengths.to(torch.int64).sum().item())
+    gi = _gen(seed_of("decode_indexer"), device)
+    qbar = torch.randn(B, 1, HEAD_DIM, generator=gi, device=device)
+    eps = torch.randn(B, HEADS, HEAD_DIM, generator=gi, device=device)
+    q = (math.sqrt(RHO) * qbar + math.sqrt(1.0 - RHO) * eps).to(torch.bfloat16)
+    w = torch.rand(B, HEADS, generator=gi, device=device)
+    bias = -0.6 * torch.rand(B, generator=gi, device=device)
+    keys = torch.randn(total, HEAD_DIM, generator=gi, device=device).to(torch.bfloat16)
+    return IndexerWorkload("decode_indexer", q, w, bias, keys, starts, lengths, starts.clone(), total, k)
+
+
+def prefill_indexer(device="cpu", rows: int = 16384, nkeys: int = 4096, k: int = 2048) -> IndexerWorkload:
+    """The prefill chunk's shape as indexer inputs: ``rows`` queries over one
+    causal sequence of ``nkeys`` shared keys (row i reads the first
+    L_i = max(1, (i+1)//4)), scores laid out contiguously."""
+    gi = _gen(seed_of("prefill_indexer"), device)
+    keys = torch.randn(nkeys, HEAD_DIM, generator=gi, device=device).to(torch.bfloat16)
+    idx = torch.arange(rows, device=device, dtype=torch.int64)
+    lengths = torch.clamp((idx + 1) // 4, min=1, max=nkeys).to(torch.int32)
+    starts = _contiguous_starts(lengths)
+    total = int(lengths.to(torch.int64).sum().item())
+    qbar = torch.randn(rows, 1, HEAD_DIM, generator=gi, device=device)
+    eps = torch.randn(rows, HEADS, HEAD_DIM, generator=gi, device=device)
+    q = (math.sqrt(RHO) * qbar + math.sqrt(1.0 - RHO) * eps).to(torch.bfloat16)
+    w = torch.rand(rows, HEADS, generator=gi, device=device)
+    bias = -0.6 * torch.rand(rows, generator=gi, device=device)
+    return IndexerWorkload("prefill_indexer", q, w, bias, keys, torch.zeros(rows, dtype=torch.int32, device=device),
+                           lengths, starts, total, k)
+
+
+INDEXER = {"decode": decode_indexer, "prefill": prefill_indexer}
