@@ -10,47 +10,68 @@
 // epilogue; b_i an optional per-row logit shift).
 //
 // Per 128-key tile the head logits are one MMA of M = 128 keys, N = 64
-// heads, K = 128: A is the key tile, B the row's query, both K-major in
-// shared memory with the 128-byte swizzle, staged by TMA.  The accumulator
-// sits in tensor memory, one lane per key and one column per head, so each
-// epilogue thread owns one key and reduces its 64 heads alone, in a fixed
-// order.  Work is split evenly by tiles: the tiles of all rows, in row order,
-// are cut into one contiguous range per CTA.
+// heads per row, K = 128: A is the key tile, B the rows' queries, both
+// K-major in shared memory with the 128-byte swizzle, staged by TMA.  An
+// aligned block of four consecutive rows that read the same key window (the
+// rows of a causal prefill chunk) is one group: its tiles take N = 256, so
+// each key tile is loaded once for four rows.  The accumulator sits in tensor
+// memory, one lane per key and one column per (row, head), so each epilogue
+// thread owns one key and reduces a row's 64 heads alone, in a fixed order.
+// Work is split evenly by tiles: the tiles of all groups, in row order, are
+// cut into one contiguous range per CTA.
 //
-// Warp roles (192 threads): warp 0 issues TMA loads (a ring of key tiles and
-// a double-buffered query), warp 1 owns the tensor memory and issues the
-// MMAs, warps 2..5 drain the accumulators (two of them, so the next tile's
-// MMAs overlap this tile's epilogue) and write the scores.  Every wait is a
-// bounded mbarrier wait.
+// Warp roles: warp 0 issues TMA loads (a ring of key tiles and a
+// double-buffered query block), warp 1 owns the tensor memory and issues the
+// MMAs, the other warps drain the accumulators (two of them, so the next
+// tile's MMAs overlap this tile's epilogue) and write the scores.  Every
+// wait is a bounded mbarrier wait.
+//
+// Two instances: IxCfg<1> never groups rows (a 4-stage ring, 16 KB query
+// buffers, 4 epilogue warps: the shape of decode, where no two rows share
+// keys and the key stream is the whole cost), IxCfg<4> groups them (a
+// 3-stage ring, 64 KB query buffers, 8 epilogue warps, two per lane quarter,
+// each taking every other row of a group).  Both are correct for any input;
+// the host picks by how often the key buffer is shared.
 
 constexpr int kIxHeads = 64;
 constexpr int kIxDim = 128;
 constexpr int kIxTile = 128;                                    // keys per tile (MMA M)
-constexpr int kIxStages = 4;                                    // key tiles in flight
-constexpr int kIxThreads = 192;
+constexpr int kIxGroup = 4;                                     // most rows sharing a key tile
 constexpr uint32_t kIxTileBytes = kIxTile * kIxDim * 2;         // 32 KB
 constexpr uint32_t kIxHalfBytes = kIxTileBytes / 2;             // 64 dims of a tile: 16 KB
-constexpr uint32_t kIxQBytes = kIxHeads * kIxDim * 2;           // 16 KB
-constexpr uint32_t kIxQHalfBytes = kIxQBytes / 2;               // 8 KB
-constexpr uint32_t kIxTmemCols = 128;                           // two 64-column accumulators
 
 // Instruction descriptor of tcgen05.mma.kind::f16: f32 accumulator (bits
 // 4-5 = 1), bf16 A and B (bits 7-9, 10-12 = 1), both K-major (bits 15, 16 =
 // 0), N / 8 in bits 17-22, M / 16 in bits 24-28.
-constexpr uint32_t kIxIdesc = (1u << 4) | (1u << 7) | (1u << 10) | ((uint32_t)(kIxHeads >> 3) << 17) |
-                              ((uint32_t)(kIxTile >> 4) << 24);
+__host__ __device__ constexpr uint32_t ix_idesc(uint32_t n)
+{
+    return (1u << 4) | (1u << 7) | (1u << 10) | ((n >> 3) << 17) | ((uint32_t)(kIxTile >> 4) << 24);
+}
 
+template <int STAGES>
 struct IxCtrl {
-    uint64_t full[kIxStages], empty[kIxStages];
+    uint64_t full[STAGES], empty[STAGES];
     uint64_t qfull[2], qempty[2];
     uint64_t afull[2], aempty[2];
     uint32_t tmem;
     uint32_t scan[32];
     uint32_t total, first_row, first_tile;
 };
-// Dynamic shared memory: [ring: kIxStages x 32 KB][query: 2 x 16 KB][IxCtrl],
-// from a 1024-byte aligned base (the 128-byte swizzle repeats every 1 KB).
-constexpr uint32_t kIxSmemBytes = kIxStages * kIxTileBytes + 2 * kIxQBytes + sizeof(IxCtrl) + 1024;
+template <int G>
+struct IxCfg {
+    static constexpr int kStages = G == 1 ? 4 : 3;              // key tiles in flight
+    static constexpr int kEpiWarps = G == 1 ? 4 : 8;
+    static constexpr int kThreads = 64 + 32 * kEpiWarps;
+    static constexpr uint32_t kQRows = G * kIxHeads;             // query rows per load
+    static constexpr uint32_t kQBytes = kQRows * kIxDim * 2;     // 16 or 64 KB
+    static constexpr uint32_t kQHalfBytes = kQBytes / 2;
+    static constexpr uint32_t kAccCols = G * kIxHeads;           // columns per accumulator
+    static constexpr uint32_t kTmemCols = 2 * kAccCols;          // 128 or 512
+    // Dynamic shared memory: [ring: kStages x 32 KB][query: 2 x kQBytes]
+    // [IxCtrl], from a 1024-byte aligned base (the 128-byte swizzle repeats
+    // every 1 KB).
+    static constexpr uint32_t kSmemBytes = kStages * kIxTileBytes + 2 * kQBytes + sizeof(IxCtrl<kStages>) + 1024;
+};
 
 struct IxParams {
     const float *w;                  // [B, 64]
@@ -135,34 +156,81 @@ __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.
 
 // ---- rows and the walk over a CTA's tiles ----------------------------------- //
 struct IxRow {
-    int r;          // row
-    uint32_t t;     // tile within the row
-    uint32_t nt;    // tiles of the row
-    int32_t L, ks, ss;
+    int r;              // the group's first row
+    uint32_t t;         // tile within the group
+    uint32_t nt;        // tiles of the group
+    uint32_t gsize;     // rows in the group (1 or kIxGroup)
+    int32_t ks;         // the group's key window start
+    int32_t L[kIxGroup], ss[kIxGroup];   // each member's valid length and score start
 };
 
-// Tiles of row r (0 for an empty or rejected row); the window checks are
-// topk_ragged's, on both the key and the score window.
-__device__ __forceinline__ uint32_t ix_row(const IxParams &p, int r, IxRow &c, uint32_t &bad)
+// Row r's own checks (topk_ragged's, on the key and the score window): its
+// valid length (0 when rejected) and its status bit.
+__device__ __forceinline__ int32_t ix_check(const IxParams &p, int r, int64_t &k0, int64_t &s0, uint32_t &bad)
 {
     int64_t len = p.lengths[r];
     if (len < 0) len = 0;
-    const int64_t k0 = p.key_starts[r], s0 = p.score_starts[r];
+    k0 = p.key_starts[r];
+    s0 = p.score_starts[r];
     bad = 0;
     if (len >= (int64_t)TOPK_RAGGED_MAX_LEN)
         bad = TOPK_DEV_LEN_ENVELOPE;
     else if (k0 < 0 || k0 + len > p.n_keys || s0 < 0 || s0 + len > p.n_scores)
         bad = TOPK_DEV_BAD_WINDOW;
+    return bad ? 0 : (int32_t)len;
+}
+
+// The work unit that starts at row r, and its tile count.  With G = 4, rows
+// 4b..4b+3 form one group when all four exist, pass their checks and start
+// at the same key; the group's later rows then have no tiles of their own.
+// Every other row is a group of one.  `bad` is row r's own status bit.
+template <int G>
+__device__ __forceinline__ uint32_t ix_row(const IxParams &p, int r, IxRow &c, uint32_t &bad)
+{
+    int64_t k0, s0;
+    const int32_t L0 = ix_check(p, r, k0, s0, bad);
+    const int b0 = r & ~(kIxGroup - 1);
+    bool grouped = G > 1 && b0 + kIxGroup <= p.B;
+    int32_t Lm[kIxGroup];
+    int64_t km[kIxGroup], sm[kIxGroup];
+    if (grouped) {
+#pragma unroll
+        for (int m = 0; m < kIxGroup; ++m) {
+            uint32_t bm;
+            Lm[m] = ix_check(p, b0 + m, km[m], sm[m], bm);
+            grouped = grouped && bm == 0 && km[m] == km[0];
+        }
+    }
     c.r = r;
-    c.L = bad ? 0 : (int32_t)len;
-    c.ks = (int32_t)k0;
-    c.ss = (int32_t)s0;
-    c.nt = (uint32_t)((c.L + kIxTile - 1) / kIxTile);
+    if (grouped) {
+        c.gsize = kIxGroup;
+        c.ks = (int32_t)km[0];
+        int32_t Lmax = 0;
+#pragma unroll
+        for (int m = 0; m < kIxGroup; ++m) {
+            c.L[m] = Lm[m];
+            c.ss[m] = (int32_t)sm[m];
+            Lmax = max(Lmax, Lm[m]);
+        }
+        c.nt = r == b0 ? (uint32_t)((Lmax + kIxTile - 1) / kIxTile) : 0u;
+    } else {
+        c.gsize = 1;
+        c.ks = (int32_t)k0;
+        c.L[0] = L0;
+        c.ss[0] = (int32_t)s0;
+#pragma unroll
+        for (int m = 1; m < kIxGroup; ++m) {
+            c.L[m] = 0;
+            c.ss[m] = 0;
+        }
+        c.nt = (uint32_t)((L0 + kIxTile - 1) / kIxTile);
+    }
     return c.nt;
 }
 
 // Next tile in row order (the caller knows one is left; the row bound is
 // a guard that the tile count makes unreachable).
+template <int G>
 __device__ __forceinline__ void ix_next(const IxParams &p, IxRow &c)
 {
     uint32_t bad;
@@ -170,25 +238,32 @@ __device__ __forceinline__ void ix_next(const IxParams &p, IxRow &c)
     c.t = 0;
     do {
         if (c.r + 1 >= p.B) {
-            c.L = 0;
+            c.gsize = 1;
+            c.L[0] = 0;
             return;
         }
-        ix_row(p, c.r + 1, c, bad);
+        ix_row<G>(p, c.r + 1, c, bad);
     } while (c.nt == 0);
 }
 
-template <int THREADS>
-__global__ void __launch_bounds__(THREADS, 1) indexer_scores_kernel(const __grid_constant__ CUtensorMap tmap_k,
-                                                                    const __grid_constant__ CUtensorMap tmap_q,
-                                                                    const IxParams p)
+template <int G>
+__global__ void __launch_bounds__(IxCfg<G>::kThreads, 1)
+    indexer_scores_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_q,
+                          const IxParams p)
 {
+    using C = IxCfg<G>;
+    constexpr int THREADS = C::kThreads;
+    constexpr int kIxStages = C::kStages;
+    constexpr int kIxEpiWarps = C::kEpiWarps;
+    constexpr uint32_t kIxQBytes = C::kQBytes, kIxQHalfBytes = C::kQHalfBytes;
+    constexpr uint32_t kIxAccCols = C::kAccCols, kIxTmemCols = C::kTmemCols;
     grid_dependency_enter();
     extern __shared__ unsigned char ix_smem_raw[];
     const uint32_t raw = smem_addr(ix_smem_raw);
     unsigned char *smem = ix_smem_raw + (((raw + 1023u) & ~1023u) - raw);
     unsigned char *ring = smem;
     unsigned char *qbuf = smem + kIxStages * kIxTileBytes;
-    IxCtrl &ctrl = *reinterpret_cast<IxCtrl *>(qbuf + 2 * kIxQBytes);
+    IxCtrl<kIxStages> &ctrl = *reinterpret_cast<IxCtrl<kIxStages> *>(qbuf + 2 * kIxQBytes);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // ---- this CTA's range of tiles ----------------------------------------- //
@@ -199,7 +274,7 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_scores_kernel(const __grid
         IxRow c;
         for (int r = lo; r < hi; ++r) {
             uint32_t bad;
-            cnt += ix_row(p, r, c, bad);
+            cnt += ix_row<G>(p, r, c, bad);
             bad_any |= bad;
         }
         if (bad_any && blockIdx.x == 0) atomicOr(&g_status, bad_any);
@@ -212,7 +287,7 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_scores_kernel(const __grid
             uint32_t before = incl - cnt;
             for (int r = lo; r < hi; ++r) {
                 uint32_t bad;
-                const uint32_t nt = ix_row(p, r, c, bad);
+                const uint32_t nt = ix_row<G>(p, r, c, bad);
                 if (first < before + nt) {
                     ctrl.first_row = (uint32_t)r;
                     ctrl.first_tile = first - before;
@@ -230,7 +305,7 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_scores_kernel(const __grid
                 mbar_init(&ctrl.qfull[s], 1);
                 mbar_init(&ctrl.qempty[s], 1);
                 mbar_init(&ctrl.afull[s], 1);
-                mbar_init(&ctrl.aempty[s], 4 * 32);
+                mbar_init(&ctrl.aempty[s], kIxEpiWarps * 32);
             }
         }
         __syncthreads();
@@ -242,7 +317,7 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_scores_kernel(const __grid
     IxRow start;
     {
         uint32_t bad;
-        ix_row(p, (int)ctrl.first_row, start, bad);
+        ix_row<G>(p, (int)ctrl.first_row, start, bad);
         start.t = ctrl.first_tile;
     }
 
@@ -264,7 +339,7 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_scores_kernel(const __grid
                     mbar_wait_bounded(&ctrl.qempty[qi], ((qn >> 1) & 1u) ^ 1u);
                     mbar_arrive_expect_tx(&ctrl.qfull[qi], kIxQBytes);
                     unsigned char *qd = qbuf + qi * kIxQBytes;
-                    tma_load_2d(qd, &tmap_q, 0, c.r * kIxHeads, &ctrl.qfull[qi]);
+                    tma_load_2d(qd, &tmap_q, 0, c.r * kIxHeads, &ctrl.qfull[qi]);   // rows r..r+G-1
                     tma_load_2d(qd + kIxQHalfBytes, &tmap_q, 64, c.r * kIxHeads, &ctrl.qfull[qi]);
                     ++qn;
                     cur = c.r;
@@ -279,7 +354,7 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_scores_kernel(const __grid
                     stage = 0;
                     sph ^= 1u;
                 }
-                if (i + 1 < n) ix_next(p, c);
+                if (i + 1 < n) ix_next<G>(p, c);
             }
         }
         __syncwarp();
@@ -303,14 +378,15 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_scores_kernel(const __grid
                 tc_fence_after();
                 const uint32_t abase = smem_addr(ring + stage * kIxTileBytes);
                 const uint32_t bbase = smem_addr(qbuf + qi * kIxQBytes);
+                const uint32_t idesc = ix_idesc(c.gsize * (uint32_t)kIxHeads);   // N = 64 per row
 #pragma unroll
                 for (int kk = 0; kk < kIxDim / 16; ++kk) {
                     // 16 dims per MMA: 32 bytes into the 128-byte swizzle row,
                     // the second 64 dims in the second half.
                     const uint32_t off_a = (uint32_t)(kk >> 2) * kIxHalfBytes + (uint32_t)(kk & 3) * 32u;
                     const uint32_t off_b = (uint32_t)(kk >> 2) * kIxQHalfBytes + (uint32_t)(kk & 3) * 32u;
-                    tc_mma(tmem + a * (uint32_t)kIxHeads, sw128_desc(abase + off_a), sw128_desc(bbase + off_b),
-                           kIxIdesc, kk > 0 ? 1u : 0u);
+                    tc_mma(tmem + a * kIxAccCols, sw128_desc(abase + off_a), sw128_desc(bbase + off_b), idesc,
+                           kk > 0 ? 1u : 0u);
                 }
                 tc_commit(&ctrl.empty[stage]);
                 tc_commit(&ctrl.afull[a]);
@@ -318,43 +394,47 @@ __global__ void __launch_bounds__(THREADS, 1) indexer_scores_kernel(const __grid
                     stage = 0;
                     sph ^= 1u;
                 }
-                if (i + 1 < n) ix_next(p, c);
+                if (i + 1 < n) ix_next<G>(p, c);
             }
         }
         __syncwarp();
     } else {
-        // ---- epilogue: one key per thread --------------------------------- //
+        // ---- epilogue: one key per thread, every other row of the group -- //
         const uint32_t quarter = (uint32_t)warp & 3u;   // the TMEM lanes this warp may read
+        const uint32_t m0 = (uint32_t)(warp - 2) >> 2;  // 0 or 1: the group rows m0, m0 + 2
         const uint32_t key_in_tile = quarter * 32u + (uint32_t)lane;
         IxRow c = start;
         for (uint32_t i = 0; i < n; ++i) {
             const uint32_t a = i & 1u;
             mbar_wait_bounded(&ctrl.afull[a], (i >> 1) & 1u);
             tc_fence_after();
-            uint32_t v0[32], v1[32];
-            const uint32_t taddr = tmem + ((quarter * 32u) << 16) + a * (uint32_t)kIxHeads;
-            tmem_ld32(taddr, v0);
-            tmem_ld32(taddr + 32u, v1);
-            tmem_wait_ld();
+            const int32_t j = (int32_t)(c.t * kIxTile + key_in_tile);
+            for (uint32_t m = m0; m < c.gsize; m += 2) {   // warp-uniform
+                uint32_t v0[32], v1[32];
+                const uint32_t taddr = tmem + ((quarter * 32u) << 16) + a * kIxAccCols + m * (uint32_t)kIxHeads;
+                tmem_ld32(taddr, v0);
+                tmem_ld32(taddr + 32u, v1);
+                tmem_wait_ld();
+                if (j < c.L[m]) {
+                    const int row = c.r + (int)m;
+                    const float b = p.bias ? __ldg(p.bias + row) : 0.0f;
+                    const float4 *wr = reinterpret_cast<const float4 *>(p.w + (int64_t)row * kIxHeads);
+                    float s = 0.0f;
+#pragma unroll
+                    for (int h4 = 0; h4 < kIxHeads / 4; ++h4) {
+                        const float4 ww = __ldg(wr + h4);
+                        const uint32_t *v = h4 < 8 ? v0 + 4 * h4 : v1 + 4 * (h4 - 8);
+                        s = fmaf(ww.x, fmaxf(fmaf(__uint_as_float(v[0]), p.scale, b), 0.0f), s);
+                        s = fmaf(ww.y, fmaxf(fmaf(__uint_as_float(v[1]), p.scale, b), 0.0f), s);
+                        s = fmaf(ww.z, fmaxf(fmaf(__uint_as_float(v[2]), p.scale, b), 0.0f), s);
+                        s = fmaf(ww.w, fmaxf(fmaf(__uint_as_float(v[3]), p.scale, b), 0.0f), s);
+                    }
+                    p.scores[(int64_t)c.ss[m] + j] = s;
+                }
+            }
             tc_fence_before();
             mbar_arrive(&ctrl.aempty[a]);
-            const int32_t j = (int32_t)(c.t * kIxTile + key_in_tile);
-            if (j < c.L) {
-                const float b = p.bias ? __ldg(p.bias + c.r) : 0.0f;
-                const float4 *wr = reinterpret_cast<const float4 *>(p.w + (int64_t)c.r * kIxHeads);
-                float s = 0.0f;
-#pragma unroll
-                for (int h4 = 0; h4 < kIxHeads / 4; ++h4) {
-                    const float4 ww = __ldg(wr + h4);
-                    const uint32_t *v = h4 < 8 ? v0 + 4 * h4 : v1 + 4 * (h4 - 8);
-                    s = fmaf(ww.x, fmaxf(fmaf(__uint_as_float(v[0]), p.scale, b), 0.0f), s);
-                    s = fmaf(ww.y, fmaxf(fmaf(__uint_as_float(v[1]), p.scale, b), 0.0f), s);
-                    s = fmaf(ww.z, fmaxf(fmaf(__uint_as_float(v[2]), p.scale, b), 0.0f), s);
-                    s = fmaf(ww.w, fmaxf(fmaf(__uint_as_float(v[3]), p.scale, b), 0.0f), s);
-                }
-                p.scores[(int64_t)c.ss + j] = s;
-            }
-            if (i + 1 < n) ix_next(p, c);
+            if (i + 1 < n) ix_next<G>(p, c);
         }
     }
 

@@ -2526,9 +2526,12 @@ int init_locked(int device)
                                               cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
             rc = TOPK_ERR_CUDA;
     }
-    if (rc == TOPK_OK && cudaFuncSetAttribute((const void *)indexer_scores_kernel<kIxThreads>,
-                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                              (int)kIxSmemBytes) != cudaSuccess)
+    if (rc == TOPK_OK && (cudaFuncSetAttribute((const void *)indexer_scores_kernel<1>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)IxCfg<1>::kSmemBytes) != cudaSuccess ||
+                          cudaFuncSetAttribute((const void *)indexer_scores_kernel<kIxGroup>,
+                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                               (int)IxCfg<kIxGroup>::kSmemBytes) != cudaSuccess))
         rc = TOPK_ERR_CUDA;
     if (rc == TOPK_OK && !g_encode_tiled) {
         void *fn = nullptr;
@@ -2779,9 +2782,13 @@ int topk_ragged_indexer_scores(const uint16_t *q, const float *w, const float *b
     if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return TOPK_ERR_CUDA;
     const int rc = ensure_init(device, cap == cudaStreamCaptureStatusNone);
     if (rc != TOPK_OK) return rc;
+    // Rows share key tiles only when the key buffer is read by more than one
+    // row on average (a causal prefill chunk); otherwise the single-row
+    // instance keeps a deeper ring for the key stream.  Either is correct.
+    const bool grouped = 2 * n_keys <= n_scores;
     CUtensorMap tmap_k, tmap_q;
     if (!encode_bf16_rows(&tmap_k, keys, (uint64_t)n_keys, kIxTile) ||
-        !encode_bf16_rows(&tmap_q, q, (uint64_t)B * kIxHeads, kIxHeads))
+        !encode_bf16_rows(&tmap_q, q, (uint64_t)B * kIxHeads, grouped ? IxCfg<kIxGroup>::kQRows : IxCfg<1>::kQRows))
         return TOPK_ERR_INVALID_ARG;
     IxParams prm;
     prm.w = w;
@@ -2796,15 +2803,17 @@ int topk_ragged_indexer_scores(const uint16_t *q, const float *w, const float *b
     prm.scale = scale;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)g_devices[device].sm_count, 1, 1);
-    cfg.blockDim = dim3((unsigned)kIxThreads, 1, 1);
-    cfg.dynamicSmemBytes = kIxSmemBytes;
+    cfg.blockDim = dim3((unsigned)(grouped ? IxCfg<kIxGroup>::kThreads : IxCfg<1>::kThreads), 1, 1);
+    cfg.dynamicSmemBytes = grouped ? IxCfg<kIxGroup>::kSmemBytes : IxCfg<1>::kSmemBytes;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, indexer_scores_kernel<kIxThreads>, tmap_k, tmap_q, prm) != cudaSuccess) {
+    const cudaError_t err = grouped ? cudaLaunchKernelEx(&cfg, indexer_scores_kernel<kIxGroup>, tmap_k, tmap_q, prm)
+                                    : cudaLaunchKernelEx(&cfg, indexer_scores_kernel<1>, tmap_k, tmap_q, prm);
+    if (err != cudaSuccess) {
         cudaGetLastError();
         return TOPK_ERR_CUDA;
     }

@@ -32,10 +32,13 @@ def _built():
     pkg.init()
 
 
-def make_case(lengths, shared_keys=False, seed=0, bias=True, rho=0.99, gap=0):
+def make_case(lengths, shared_keys=False, seed=0, bias=True, rho=0.99, gap=0, score_gap=3, extra_keys=0):
     """Correlated-head queries (as the workloads' indexer), U(0,1) head
     weights, N(0,1) bf16 keys; decode layout (own keys per row) or a causal
-    prefill layout (every row reads the first L_i keys)."""
+    prefill layout (every row reads the first L_i keys).  Score windows are
+    score_gap apart.  The library groups rows that share key tiles when the
+    score buffer holds at least twice as many entries as the key buffer has
+    rows, so score_gap also picks which of its two kernels runs."""
     g = torch.Generator().manual_seed(seed)
     B = len(lengths)
     lengths = torch.tensor(lengths, dtype=torch.int32)
@@ -50,10 +53,11 @@ def make_case(lengths, shared_keys=False, seed=0, bias=True, rho=0.99, gap=0):
         key_starts = torch.zeros(B, dtype=torch.int32)
         key_starts[1:] = torch.cumsum(lengths + gap, 0)[:-1].to(torch.int32)
         n_keys = max(1, int((lengths + gap).sum()))
+    n_keys += extra_keys
     keys = torch.randn(n_keys, D, generator=g).to(torch.bfloat16)
     score_starts = torch.zeros(B, dtype=torch.int32)
-    score_starts[1:] = torch.cumsum(lengths + 3, 0)[:-1].to(torch.int32)
-    n_scores = int((lengths + 3).sum())
+    score_starts[1:] = torch.cumsum(lengths + score_gap, 0)[:-1].to(torch.int32)
+    n_scores = int((lengths + score_gap).sum())
     return dict(q=q, w=w, bias=b, keys=keys, key_starts=key_starts, lengths=lengths,
                 score_starts=score_starts, n_scores=n_scores)
 
@@ -186,3 +190,37 @@ def test_graph_capture_of_the_chain():
     gr.replay()
     torch.cuda.synchronize()
     assert torch.equal(idx, ref)
+
+
+def test_row_groups_and_their_edges():
+    # Aligned blocks of four rows that read the same key window share key
+    # tiles; blocks that break the rule (another key start, a rejected row,
+    # a batch that is not a multiple of four) fall back to single rows.
+    c = make_case([300, 299, 0, 1000, 7, 7, 7, 7, 50, 4000, 129, 128, 5, 6, 70], shared_keys=True, seed=10,
+                  score_gap=1000)
+    assert 2 * c["keys"].shape[0] <= c["n_scores"]                               # the grouping kernel
+    c["key_starts"][4:8] = torch.tensor([0, 0, 1, 0], dtype=torch.int32)      # block 1: one start differs
+    assert_scores(c)
+    d = make_case([500, 400, 300, 200, 100, 90, 80, 70], shared_keys=True, seed=11)
+    assert 2 * d["keys"].shape[0] <= d["n_scores"]
+    d["score_starts"][6] = d["n_scores"] - 10                                    # block 1: row 6 rejected
+    pkg.device_status()
+    got = gpu_scores(d)
+    want, written, mag = oracle_scores(d, 1.0 / D ** 0.5)
+    ok = written & (got != SENTINEL)
+    assert written[:d["score_starts"][6]].sum() > 0 and pkg.device_status() == pkg.TOPK_DEV_BAD_WINDOW
+    assert np.all(np.abs(got[ok] - want[ok]) <= 2.0 ** -16 * mag[ok] + 1e-30)
+    assert (got[written] != SENTINEL).all()
+
+
+@pytest.mark.parametrize("shared,score_gap,extra_keys,grouping", [
+    (False, 0, 0, False),          # own keys per row, the single-row kernel
+    (False, 12000, 0, True),       # own keys per row through the grouping kernel (no group forms)
+    (True, 0, 40000, False),       # shared keys through the single-row kernel
+    (True, 0, 0, True),            # shared keys, grouped
+])
+def test_both_kernels_on_the_same_rows(shared, score_gap, extra_keys, grouping):
+    lengths = [max(1, (i + 1) // 3) * 37 % 3000 + 1 for i in range(64)]
+    c = make_case(lengths, shared_keys=shared, seed=12, score_gap=score_gap, extra_keys=extra_keys)
+    assert (2 * c["keys"].shape[0] <= c["n_scores"]) == grouping
+    assert_scores(c)
