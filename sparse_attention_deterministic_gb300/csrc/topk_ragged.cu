@@ -2203,15 +2203,189 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
 }
 
 // ------------------------------------------------------------------------- //
-// Tie / plateau statistics of each row at its k-th boundary, one CTA per
-// row.  The radix select of the top-k kernels, with every pass reading the
+// Tie / plateau statistics of each row at its k-th boundary, one cluster of
+// CS CTAs per row (CS = 1..16, from B on the host).  The radix select of the
+// top-k kernels, every pass reading the row from global memory: each CTA
+// bins its contiguous slice, the cluster's histograms are summed over DSMEM
+// after a cluster barrier, and every CTA makes the same selection from the
+// same integers.  The top 11, next 11 and last 10 bits of the order key
+// narrow the bin holding the k-th key down to the key itself; the entries
+// above it and equal to it are the counts above and inside the last bin.
+// Levels 0 and 2 use one histogram buffer and level 1 the other, so one
+// cluster barrier per level keeps every CTA's reads ahead of the next
+// clear.  A row no longer than k takes one pass (its 0.0 count).
+// ------------------------------------------------------------------------- //
+constexpr int kStatsThreads = 512;
+
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS) topk_stats_cluster_kernel(const float *scores, int64_t n_scores,
+                                                                     const int32_t *row_starts,
+                                                                     const int32_t *lengths, int32_t k,
+                                                                     topk_row_stats *out)
+{
+    grid_dependency_enter();
+    constexpr int BPT = kBins / THREADS;
+    static_assert(BPT == 4, "four bins per thread: one 16-byte DSMEM load per peer");
+    constexpr uint32_t kNone = 0xFFFFFFFFu;
+    __shared__ __align__(16) uint32_t hist[2][kBins];
+    __shared__ uint32_t scan[32];
+    __shared__ uint32_t sel[3];   // selected digit, entries above its bin, entries in it
+    __shared__ uint32_t zeros;    // this CTA's 0.0 count
+    const int tid = threadIdx.x, lane = tid & 31;
+    const uint32_t crank = cluster_rank(), csize = cluster_size();
+    const int row = (int)(blockIdx.x / csize);
+
+    topk_row_stats res = {0u, 0u, 0u, 0u, 0u, 0u};
+    const int64_t rs = row_starts[row];
+    int64_t len = lengths[row];
+    if (len < 0) len = 0;
+    uint32_t bad = 0;
+    if (len >= (int64_t)TOPK_RAGGED_MAX_LEN)
+        bad = TOPK_DEV_LEN_ENVELOPE;
+    else if (rs < 0 || rs + len > n_scores)
+        bad = TOPK_DEV_BAD_WINDOW;
+    if (bad) {   // the same for every CTA of the cluster: none touches another's memory
+        if (crank == 0 && tid == 0) {
+            atomicOr(&g_status, bad);
+            out[row] = res;
+        }
+        return;
+    }
+    const uint32_t L = (uint32_t)len;
+    const bool has_boundary = L > (uint32_t)k;
+
+    // This CTA's slice as [head | 16-byte aligned quads | tail]; head and
+    // tail hold fewer than four entries each.
+    const uint32_t lo = (uint32_t)((uint64_t)L * crank / csize);
+    const uint32_t Ls = (uint32_t)((uint64_t)L * (crank + 1) / csize) - lo;
+    const float *x = scores + rs + lo;
+    const uint32_t *xs = reinterpret_cast<const uint32_t *>(x);
+    const uint32_t head = min(Ls, (4u - (uint32_t)(((uintptr_t)x >> 2) & 3u)) & 3u);
+    const uint32_t nq = (Ls - head) >> 2;
+    const uint32_t tail0 = head + 4u * nq;
+    const uint4 *xq = reinterpret_cast<const uint4 *>(x + head);
+
+    if (tid == 0) zeros = 0u;
+    uint32_t prefix = 0, above = 0, r = (uint32_t)k, tie = 0;
+    bool failed = false;
+    const int levels = has_boundary ? 3 : 1;
+    for (int level = 0; level < levels; ++level) {
+        const int dsh = level == 0 ? 21 : (level == 1 ? 10 : 0);   // digit shift
+        const int dbits = level == 2 ? 10 : 11;
+        const uint32_t dmask = (1u << dbits) - 1u;
+        uint32_t *H = hist[level == 1 ? 1 : 0];
+        for (int b = tid; b < kBins; b += THREADS) H[b] = 0u;
+        if (tid == 0) {
+            sel[0] = kNone;
+            sel[1] = 0u;
+            sel[2] = 0u;
+        }
+        __syncthreads();
+
+        // Level 0 counts 0.0 entries and bins every entry; later levels bin
+        // the entries whose higher bits equal the selected prefix.
+        uint32_t nz = 0;
+        auto visit = [&](uint32_t u) {
+            const uint32_t key = order_key(u);
+            if (level == 0) {
+                nz += (u & 0x7FFFFFFFu) == 0u;
+                if (has_boundary) atomicAdd(&H[key >> 21], 1u);
+            } else if ((key >> (dsh + dbits)) == prefix) {
+                atomicAdd(&H[(key >> dsh) & dmask], 1u);
+            }
+        };
+        if ((uint32_t)tid < head) visit(xs[tid]);
+        for (uint32_t q = (uint32_t)tid; q < nq; q += 4u * THREADS) {
+            uint4 v[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t)
+                v[t] = q + t * THREADS < nq ? __ldg(xq + q + t * THREADS) : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                if (q + t * THREADS < nq) {
+                    visit(v[t].x);
+                    visit(v[t].y);
+                    visit(v[t].z);
+                    visit(v[t].w);
+                }
+            }
+        }
+        if (tail0 + (uint32_t)tid < Ls) visit(xs[tail0 + tid]);
+        if (level == 0) {
+            nz = __reduce_add_sync(kFull, nz);
+            if (lane == 0 && nz) atomicAdd(&zeros, nz);
+        }
+        cluster_sync();   // every CTA's histogram (and 0.0 count) of this level is final
+        if (!has_boundary) break;
+
+        // The cluster's bins, top first: thread t holds bins kBins-1-4t down
+        // to kBins-4(t+1), summed over the cluster's CTAs in rank order.
+        uint32_t h[BPT] = {0u, 0u, 0u, 0u};
+        const uint32_t *hb = &H[kBins - BPT * (tid + 1)];
+        for (uint32_t q = 0; q < csize; ++q) {
+            uint32_t v[4];
+            dsmem_ld_bins(dsmem_addr(hb, q), v);
+            h[0] += v[3];
+            h[1] += v[2];
+            h[2] += v[1];
+            h[3] += v[0];
+        }
+        const uint32_t sum = h[0] + h[1] + h[2] + h[3];
+        uint32_t run = block_incl_scan<THREADS>(sum, scan) - sum;
+#pragma unroll
+        for (int i = 0; i < BPT; ++i) {
+            if (run < r && run + h[i] >= r) {   // the bin where the count from the top reaches r
+                sel[0] = (uint32_t)(kBins - 1 - (BPT * tid + i));
+                sel[1] = run;
+                sel[2] = h[i];
+            }
+            run += h[i];
+        }
+        __syncthreads();
+        const uint32_t d = sel[0];
+        if (d == kNone) {   // cannot happen: the selected bin always holds >= r entries
+            failed = true;
+            break;
+        }
+        above += sel[1];
+        r -= sel[1];
+        prefix = (prefix << dbits) | d;
+        if (level == 2) tie = sel[2];
+        __syncthreads();   // every thread has read sel
+    }
+    if (crank == 0 && tid == 0) {
+        uint32_t nzero = 0;
+        for (uint32_t q = 0; q < csize; ++q) nzero += dsmem_ld(dsmem_addr(&zeros, q));
+        if (failed) {
+            atomicOr(&g_status, TOPK_DEV_INTERNAL);
+        } else {
+            res.len = L;
+            res.n_zero = nzero;
+            if (has_boundary) {
+                const uint32_t T = prefix;   // the k-th key
+                res.boundary_bits = key_bits(T);
+                res.tie = tie;
+                res.above = above;
+                res.flags = TOPK_STAT_HAS_BOUNDARY;
+                if (tie > 1u && above + tie > (uint32_t)k) res.flags |= TOPK_STAT_STRADDLE;
+                if ((res.boundary_bits & 0x7FFFFFFFu) == 0u) res.flags |= TOPK_STAT_ZERO_BOUND;
+            } else {
+                res.above = L;
+            }
+        }
+        out[row] = res;
+    }
+    cluster_sync();   // no CTA leaves while a peer may still read its shared memory
+}
+
+// ------------------------------------------------------------------------- //
+// The one-CTA form of the statistics kernel, for batches of many rows (or
+// short ones): one CTA per row.  The radix select of the top-k kernels, with every pass reading the
 // row from global memory: the top 11, next 11 and last 10 bits of the order
 // key narrow the bin holding the k-th key down to the key itself, and the
 // entries above it and equal to it are the counts above and inside the last
 // bin.  A row no longer than k takes one pass (its 0.0 count).
 // ------------------------------------------------------------------------- //
-constexpr int kStatsThreads = 512;
-
 template <int THREADS>
 __global__ void __launch_bounds__(THREADS) topk_stats_kernel(const float *scores, int64_t n_scores,
                                                              const int32_t *row_starts, const int32_t *lengths,
@@ -2526,6 +2700,9 @@ int init_locked(int device)
                                               cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
             rc = TOPK_ERR_CUDA;
     }
+    if (rc == TOPK_OK && cudaFuncSetAttribute((const void *)topk_stats_cluster_kernel<kStatsThreads>,
+                                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        rc = TOPK_ERR_CUDA;
     if (rc == TOPK_OK && (cudaFuncSetAttribute((const void *)indexer_scores_kernel<1>,
                                                cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                (int)IxCfg<1>::kSmemBytes) != cudaSuccess ||
@@ -2743,17 +2920,33 @@ int topk_ragged_stats(const float *scores, int64_t n_scores, const int32_t *row_
     if (cudaStreamIsCapturing(st, &cap) != cudaSuccess) return TOPK_ERR_CUDA;
     const int rc = ensure_init(device, cap == cudaStreamCaptureStatusNone);
     if (rc != TOPK_OK) return rc;
+    // One cluster per row: a batch of few, long rows splits each row over up
+    // to 16 CTAs, so that the batch covers about two CTAs per SM and every
+    // CTA keeps at least 16 K scores on average; otherwise one CTA per row.
+    int cs = 1;
+    while (cs < 16 && (int64_t)B * cs * 2 <= 2LL * g_devices[device].sm_count &&
+           n_scores >= (int64_t)B * cs * 2 * 16384)
+        cs *= 2;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)B, 1, 1);
+    cfg.gridDim = dim3((unsigned)((int64_t)B * cs), 1, 1);
     cfg.blockDim = dim3((unsigned)kStatsThreads, 1, 1);
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = (unsigned)cs;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    if (cudaLaunchKernelEx(&cfg, topk_stats_kernel<kStatsThreads>, scores, n_scores, row_starts, lengths, k,
-                           out) != cudaSuccess) {
+    cfg.numAttrs = 2;
+    if (cs == 1) cfg.numAttrs = 1;   // no cluster
+    const cudaError_t err =
+        cs == 1 ? cudaLaunchKernelEx(&cfg, topk_stats_kernel<kStatsThreads>, scores, n_scores, row_starts, lengths,
+                                     k, out)
+                : cudaLaunchKernelEx(&cfg, topk_stats_cluster_kernel<kStatsThreads>, scores, n_scores, row_starts,
+                                     lengths, k, out);
+    if (err != cudaSuccess) {
         cudaGetLastError();
         return TOPK_ERR_CUDA;
     }

@@ -115,3 +115,15 @@ def test_repeatable_and_graph_replay():
         assert torch.equal(out, a)
     for _ in range(3):
         assert torch.equal(pkg.topk_ragged_stats(w.scores, w.row_starts, w.lengths, w.k), a)
+
+
+def test_rejected_and_empty_rows_in_clusters():
+    # Few long rows: the library splits each over a cluster of CTAs.
+    g = torch.Generator().manual_seed(21)
+    buf = torch.relu(torch.randn(3_000_000, generator=g) - 0.5)
+    starts = torch.tensor([0, -5, 2_000_000, 100, 2_999_000, 7], dtype=torch.int32)
+    lengths = torch.tensor([900_000, 10, 999_999, 0, 5_000, 1 << 24], dtype=torch.int32)
+    for k in (1, 2048, 4096):
+        got = assert_stats(W.Workload("bad_cluster", buf, starts, lengths, k, 0, {}))
+        assert got[[1, 4, 5]].tolist() == [[0] * 6] * 3
+        assert got[3].tolist() == [0, 0, 0, 0, 0, 0]
