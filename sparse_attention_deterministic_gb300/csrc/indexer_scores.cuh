@@ -53,9 +53,10 @@ struct IxCtrl {
     uint64_t full[STAGES], empty[STAGES];
     uint64_t qfull[2], qempty[2];
     uint64_t afull[2], aempty[2];
+    uint64_t scan64[32];
     uint32_t tmem;
-    uint32_t scan[32];
-    uint32_t total, first_row, first_tile;
+    uint32_t first_row, first_tile;
+    uint32_t edge[2];   // tile indices (in row order) that open this CTA's range and the next
 };
 template <int G>
 struct IxCfg {
@@ -67,6 +68,10 @@ struct IxCfg {
     static constexpr uint32_t kQHalfBytes = kQBytes / 2;
     static constexpr uint32_t kAccCols = G * kIxHeads;           // columns per accumulator
     static constexpr uint32_t kTmemCols = 2 * kAccCols;          // 128 or 512
+    // What a work unit's query load costs, in tiles: the split of the batch
+    // weighs each unit as its tiles plus this, so CTAs that draw many short
+    // units (the first rows of a causal chunk) draw fewer tiles.
+    static constexpr uint32_t kUnitCost = G == 1 ? 1 : 4;
     // Dynamic shared memory: [ring: kStages x 32 KB][query: 2 x kQBytes]
     // [IxCtrl], from a 1024-byte aligned base (the 128-byte swizzle repeats
     // every 1 KB).
@@ -267,33 +272,49 @@ __global__ void __launch_bounds__(IxCfg<G>::kThreads, 1)
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // ---- this CTA's range of tiles ----------------------------------------- //
+    // Per thread, a contiguous run of rows: its tiles and its weight (tiles
+    // plus kUnitCost per work unit), then one 64-bit scan over the CTA.  CTA
+    // b takes the tiles whose weighted positions fall in [b W / grid,
+    // (b + 1) W / grid), a unit's cost counted before its first tile.
     {
         const int per = (p.B + THREADS - 1) / THREADS;
         const int lo = min(p.B, tid * per), hi = min(p.B, lo + per);
-        uint32_t cnt = 0, bad_any = 0;
+        uint64_t cnt = 0;   // weight << 32 | tiles
+        uint32_t bad_any = 0;
         IxRow c;
         for (int r = lo; r < hi; ++r) {
             uint32_t bad;
-            cnt += ix_row<G>(p, r, c, bad);
+            const uint32_t nt = ix_row<G>(p, r, c, bad);
+            cnt += ((uint64_t)(nt ? nt + C::kUnitCost : 0u) << 32) | nt;
             bad_any |= bad;
         }
         if (bad_any && blockIdx.x == 0) atomicOr(&g_status, bad_any);
-        const uint32_t incl = block_incl_scan<THREADS>(cnt, ctrl.scan);
-        if (tid == THREADS - 1) ctrl.total = incl;
+        uint64_t tot;
+        const uint64_t incl = block_incl_scan64<THREADS>(cnt, ctrl.scan64, tot);
+        const uint64_t excl = incl - cnt;
+        const uint32_t W = (uint32_t)(tot >> 32);
+        if (tid == 0) ctrl.edge[0] = ctrl.edge[1] = (uint32_t)tot;   // a position at W: past the last tile
         __syncthreads();
-        const uint32_t total = ctrl.total;
-        const uint32_t first = (uint32_t)((uint64_t)blockIdx.x * total / gridDim.x);
-        if (first < total && incl - cnt <= first && first < incl) {
-            uint32_t before = incl - cnt;
-            for (int r = lo; r < hi; ++r) {
-                uint32_t bad;
-                const uint32_t nt = ix_row<G>(p, r, c, bad);
-                if (first < before + nt) {
-                    ctrl.first_row = (uint32_t)r;
-                    ctrl.first_tile = first - before;
-                    break;
+        for (int e = 0; e < 2; ++e) {
+            const uint32_t pos = (uint32_t)((uint64_t)(blockIdx.x + e) * W / gridDim.x);
+            if (pos < W && (uint32_t)(excl >> 32) <= pos && pos < (uint32_t)(incl >> 32)) {
+                uint32_t pw = (uint32_t)(excl >> 32), pt = (uint32_t)excl;
+                for (int r = lo; r < hi; ++r) {
+                    uint32_t bad;
+                    const uint32_t nt = ix_row<G>(p, r, c, bad);
+                    const uint32_t wt = nt ? nt + C::kUnitCost : 0u;
+                    if (pos < pw + wt) {
+                        const uint32_t t = pos - pw < C::kUnitCost ? 0u : pos - pw - C::kUnitCost;
+                        ctrl.edge[e] = pt + t;
+                        if (e == 0) {
+                            ctrl.first_row = (uint32_t)r;
+                            ctrl.first_tile = t;
+                        }
+                        break;
+                    }
+                    pw += wt;
+                    pt += nt;
                 }
-                before += nt;
             }
         }
         if (tid == 0) {
@@ -310,9 +331,7 @@ __global__ void __launch_bounds__(IxCfg<G>::kThreads, 1)
         }
         __syncthreads();
     }
-    const uint32_t total = ctrl.total;
-    const uint32_t first = (uint32_t)((uint64_t)blockIdx.x * total / gridDim.x);
-    const uint32_t n = (uint32_t)((uint64_t)(blockIdx.x + 1) * total / gridDim.x) - first;
+    const uint32_t n = ctrl.edge[1] - ctrl.edge[0];
     if (n == 0) return;   // uniform: nothing allocated yet
     IxRow start;
     {
