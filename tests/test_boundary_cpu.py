@@ -106,3 +106,33 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(_native, "_lib", None)
     with pytest.raises(RuntimeError, match="not built"):
         _native.lib()
+
+
+def _ix_args(**kw):
+    a = dict(q=0x10000, w=0x20000, bias=None, keys=0x30000, n_keys=100, ks=0x40000, ln=0x50000, ss=0x60000,
+             B=2, scale=0.088, scores=0x70000, n_scores=1000)
+    a.update(kw)
+    return (a["q"], a["w"], a["bias"], a["keys"], a["n_keys"], a["ks"], a["ln"], a["ss"], a["B"], a["scale"],
+            a["scores"], a["n_scores"])
+
+
+@pytest.mark.parametrize("kw", [
+    dict(B=-1), dict(n_keys=0), dict(n_keys=1 << 31), dict(n_scores=-1), dict(n_scores=1 << 31),
+    dict(B=1 << 25), dict(scale=float("nan")), dict(scale=float("inf")), dict(q=None), dict(w=None),
+    dict(keys=None), dict(ks=None), dict(ln=None), dict(ss=None), dict(scores=None), dict(q=0x10008),
+    dict(keys=0x30004), dict(w=0x20004), dict(bias=0x2), dict(scores=0x70002),
+])
+def test_indexer_invalid_arguments_rejected_on_host(so, kw):
+    # Pointers here are never dereferenced: validation fails first.
+    assert so.topk_ragged_indexer_scores(*_ix_args(**kw), None) == 1
+    assert so.topk_ragged_indexer(*_ix_args(**kw), 2048, 0, 0x80000, None, None) == 1
+
+
+@pytest.mark.parametrize("k,flags,oi", [(0, 0, 0x80000), (4097, 0, 0x80000), (16, 1, 0x80000), (16, 4, 0x80000),
+                                        (16, 0, None)])
+def test_indexer_chain_selection_arguments_rejected(so, k, flags, oi):
+    assert so.topk_ragged_indexer(*_ix_args(), k, flags, oi, None, None) == 1
+
+
+def test_indexer_empty_batch_is_ok_without_device(so):
+    assert so.topk_ragged_indexer_scores(*_ix_args(B=0, q=None, w=None, ks=None, ln=None, ss=None), None) == 0
