@@ -428,12 +428,21 @@ __global__ void __launch_bounds__(IxCfg<G>::kThreads, 1)
             mbar_wait_bounded(&ctrl.afull[a], (i >> 1) & 1u);
             tc_fence_after();
             const int32_t j = (int32_t)(c.t * kIxTile + key_in_tile);
+            bool released = false;
             for (uint32_t m = m0; m < c.gsize; m += 2) {   // warp-uniform
                 uint32_t v0[32], v1[32];
                 const uint32_t taddr = tmem + ((quarter * 32u) << 16) + a * kIxAccCols + m * (uint32_t)kIxHeads;
                 tmem_ld32(taddr, v0);
                 tmem_ld32(taddr + 32u, v1);
                 tmem_wait_ld();
+                if (m + 2 >= c.gsize) {
+                    // This warp's last read of the accumulator is in registers:
+                    // release it before the arithmetic, so the MMAs of the
+                    // tile after next can start.
+                    tc_fence_before();
+                    mbar_arrive(&ctrl.aempty[a]);
+                    released = true;
+                }
                 if (j < c.L[m]) {
                     const int row = c.r + (int)m;
                     const float b = p.bias ? __ldg(p.bias + row) : 0.0f;
@@ -451,8 +460,10 @@ __global__ void __launch_bounds__(IxCfg<G>::kThreads, 1)
                     p.scores[(int64_t)c.ss[m] + j] = s;
                 }
             }
-            tc_fence_before();
-            mbar_arrive(&ctrl.aempty[a]);
+            if (!released) {   // a warp with no row of this group
+                tc_fence_before();
+                mbar_arrive(&ctrl.aempty[a]);
+            }
             if (i + 1 < n) ix_next<G>(p, c);
         }
     }
