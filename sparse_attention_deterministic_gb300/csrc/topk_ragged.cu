@@ -10,26 +10,44 @@
 // bitonic sort of 24-bit-index composites) was written for other hardware;
 // this file keeps its semantics and restructures the work for GB300:
 //
-//   * one row per thread-block cluster of C CTAs (C = 1..16, chosen from B
-//     on the host); each CTA owns a contiguous, 16-byte-aligned slice of the
-//     row and keeps as much of it as fits in shared memory, so the row is
-//     read from HBM once; the rest of a very long slice is re-read from L2;
+//   * each thread-block cluster of C CTAs (C = 2..16, chosen on the host)
+//     takes a group of rows, and every row a contiguous group of the
+//     cluster's CTAs; each CTA owns a contiguous, 16-byte-aligned slice of
+//     the row and stages as much of it as fits in shared memory (TMA bulk
+//     copies), so the row is read from HBM once; the rest of a very long
+//     slice is re-read from L2;
 //   * an MSB-first radix select on the monotone uint32 order key with digits
 //     of 11, 11 and 10 bits; per-CTA histograms use shared-memory atomics
-//     (colliding lanes are merged by the hardware) and are merged into the cluster
-//     leader through distributed shared memory (red.shared::cluster), so the
+//     (colliding lanes are merged by the hardware), and after a cluster
+//     barrier every CTA of the row's group pulls the group's histograms over
+//     distributed shared memory and makes the same threshold search, so the
 //     k-th key T, the count above it and the count needed from its tie set
 //     are exact integers, independent of scheduling;
 //   * every entry above T is a winner; entries equal to T are ranked by
 //     index with ordered per-warp / per-CTA prefix counts (the tie set is
 //     taken in index order, so its first r members are the smallest indices,
 //     and they already sit in canonical order after the winners);
-//   * the winners (fewer than k) are gathered into the leader as unique
-//     (key << 32 | ~index) composites and sorted descending in shared
-//     memory; the row is written with coalesced stores.
+//   * the winners are gathered into the row's leader CTA as unique
+//     (key << 32 | ~index) composites and sorted descending in shared memory
+//     (a counting bucket sort, bitonic only on skewed keys); the row is
+//     written with coalesced stores.
+//
+// Batches of many rows (or of short ones) take a one-CTA-per-row kernel
+// instead (topk_row_kernel): rows of up to 4096 scores are ranked from
+// registers by one bucket pass split at +0.0, longer ones by the same radix
+// select over shared memory.
+//
+// The same file holds the operations around the selection: the page-table
+// transform of the output (a pass over each finished row, in the same
+// launch), the per-row tie / plateau statistics (topk_stats_kernel and its
+// cluster form), and, from indexer_scores.cuh, the lightning-indexer scores
+// on the tcgen05 tensor cores.
 //
 // Nothing is allocated; the only global state is a status word for data
-// errors.  All cross-CTA synchronisation uses hardware cluster barriers.
+// errors.  Cross-CTA synchronisation uses hardware cluster barriers, and
+// every mbarrier wait has an iteration limit.  Every kernel starts with a
+// programmatic-dependent-launch wait, so it touches no global memory before
+// the grids ahead of it in the stream have finished.
 
 #include <cuda.h>
 #include <cudaTypedefs.h>
