@@ -554,10 +554,19 @@ __device__ void sort_and_write(uint64_t *a, uint64_t *b, int n, int n_out, int c
 
 __device__ __forceinline__ void pad_out(int32_t *oi, float *ov, int from, int to)
 {
-    for (int p = from + (int)threadIdx.x; p < to; p += (int)blockDim.x) {
-        oi[p] = -1;
-        if (ov) ov[p] = __uint_as_float(kNegInfBits);
-    }
+    if (from >= to) return;
+    const int t = (int)threadIdx.x, nt = (int)blockDim.x;
+    // Indices: 16-byte stores over the aligned middle, single stores over
+    // the (fewer than four) entries before and after it.
+    int a = from + (int)((4u - (uint32_t)(((uintptr_t)(oi + from) >> 2) & 3u)) & 3u);
+    if (a > to) a = to;
+    const int nv = (to - a) >> 2, tail = a + 4 * nv;
+    if (t < a - from) oi[from + t] = -1;
+    if (t < to - tail) oi[tail + t] = -1;
+    int4 *o4 = reinterpret_cast<int4 *>(oi + a);
+    for (int q = t; q < nv; q += nt) o4[q] = make_int4(-1, -1, -1, -1);
+    if (ov)
+        for (int p = from + t; p < to; p += nt) ov[p] = __uint_as_float(kNegInfBits);
 }
 
 // ------------------------------------------------------------------------- //
