@@ -192,7 +192,7 @@ int topk_ragged_stats(const float *scores, int64_t n_scores, const int32_t *row_
  * w             device fp32 [B][64], 16-byte aligned.
  * bias          device fp32 [B], or NULL for 0.
  * keys          device, bf16 bit patterns, [n_keys][128], 16-byte aligned;
- *               1 <= n_keys < 2^31.
+ *               1 <= n_keys <= 2^31 - 128.
  * key_starts, lengths, score_starts
  *               device int32 [B]: row i reads keys[key_starts[i] + j] and
  *               writes scores[score_starts[i] + j] for j < L_i (a negative

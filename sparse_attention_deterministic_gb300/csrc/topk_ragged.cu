@@ -2985,7 +2985,9 @@ int topk_ragged_indexer_scores(const uint16_t *q, const float *w, const float *b
                                const int32_t *score_starts, int32_t B, float scale, float *scores, int64_t n_scores,
                                void *stream)
 {
-    if (B < 0 || n_keys < 1 || n_keys >= ((int64_t)1 << 31) || n_scores < 0 || n_scores >= ((int64_t)1 << 31))
+    // n_keys leaves room for a last partial tile's row coordinate in int32.
+    if (B < 0 || n_keys < 1 || n_keys > ((int64_t)1 << 31) - kIxTile || n_scores < 0 ||
+        n_scores >= ((int64_t)1 << 31))
         return TOPK_ERR_INVALID_ARG;
     if ((int64_t)B * kIxHeads >= ((int64_t)1 << 31) || !(scale == scale) || scale > 3.0e38f || scale < -3.0e38f)
         return TOPK_ERR_INVALID_ARG;

@@ -117,7 +117,7 @@ def _ix_args(**kw):
 
 
 @pytest.mark.parametrize("kw", [
-    dict(B=-1), dict(n_keys=0), dict(n_keys=1 << 31), dict(n_scores=-1), dict(n_scores=1 << 31),
+    dict(B=-1), dict(n_keys=0), dict(n_keys=1 << 31), dict(n_keys=(1 << 31) - 127), dict(n_scores=-1), dict(n_scores=1 << 31),
     dict(B=1 << 25), dict(scale=float("nan")), dict(scale=float("inf")), dict(q=None), dict(w=None),
     dict(keys=None), dict(ks=None), dict(ln=None), dict(ss=None), dict(scores=None), dict(q=0x10008),
     dict(keys=0x30004), dict(w=0x20004), dict(bias=0x2), dict(scores=0x70002),
