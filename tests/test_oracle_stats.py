@@ -167,3 +167,32 @@ def test_planted_slip_is_caught(name):
         except (AssertionError, IndexError):
             failed.append(pin.__name__)
     assert failed, f"no pin caught {name}"
+
+
+# --------------------------------------------------------------------------- #
+# Closed forms of the sglang page's tie-safety families: a plateau row of m
+# distinct positives and L - m exact zeros has, for m < k, its boundary on
+# the zero plateau with a tie set of L - m; a tie block of T copies of 1.0
+# placed so that k - T//2 distinct larger values sit above it has the
+# boundary 1.0 with tie T and above k - T//2.
+# --------------------------------------------------------------------------- #
+@pytest.mark.parametrize("m", [0, 1, 256, 1024, 2047])
+def test_plateau_family_closed_form(m):
+    L, k = 8192, 2048
+    w = W.plateau(3, L, m, k)
+    s, st, ln = w.numpy()
+    stats, fl = oracle.row_stats(s, st, ln, k)
+    assert not fl.any()
+    for row in stats.tolist():
+        assert row == [L, L - m, 0, L - m, m, HAS | STR | ZB]
+
+
+@pytest.mark.parametrize("T", [2, 64, 512, 4096])
+def test_tie_block_family_closed_form(T):
+    L, k = 16384, 2048
+    w = W.tie_block(3, L, k, T)
+    s, st, ln = w.numpy()
+    stats, _ = oracle.row_stats(s, st, ln, k)
+    above = max(0, k - T // 2)
+    for row in stats.tolist():
+        assert row == [L, 0, 0x3F800000, T, above, HAS | STR]
