@@ -18,6 +18,13 @@
  *   - output rows are front-packed: the min(k, L_i) selected indices in
  *     canonical order, then -1.
  *
+ * Around the selection the library offers its neighbours in the indexer
+ * pipeline: the selection written as KV-cache slots through a page table
+ * (topk_ragged_paged), per-row tie / plateau statistics at the k-th boundary
+ * (topk_ragged_stats), and the indexer scores themselves on the tcgen05
+ * tensor cores, alone or chained with the selection (topk_ragged_indexer_scores,
+ * topk_ragged_indexer).
+ *
  * Every call is stream-ordered and asynchronous, allocates nothing, and may be
  * captured into a CUDA graph once topk_ragged_init() has run for the device.
  * Results are bitwise identical from run to run and independent of which

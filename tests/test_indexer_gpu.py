@@ -224,3 +224,17 @@ def test_both_kernels_on_the_same_rows(shared, score_gap, extra_keys, grouping):
     c = make_case(lengths, shared_keys=shared, seed=12, score_gap=score_gap, extra_keys=extra_keys)
     assert (2 * c["keys"].shape[0] <= c["n_scores"]) == grouping
     assert_scores(c)
+
+
+def test_scores_do_not_depend_on_the_kernel_instance():
+    # The same shared-key rows, once grouped (four rows per MMA, N = 256) and
+    # once one row per MMA (N = 64, forced by a larger key buffer): the fp32
+    # scores must agree bit for bit, so a row's scores do not depend on the
+    # rest of its batch.
+    lengths = [max(1, (i + 1) // 3) * 37 % 3000 + 1 for i in range(64)]
+    grouped = make_case(lengths, shared_keys=True, seed=13)
+    single = dict(grouped)
+    single["keys"] = torch.cat([grouped["keys"], torch.zeros(40000, D, dtype=torch.bfloat16)])
+    assert 2 * grouped["keys"].shape[0] <= grouped["n_scores"] < 2 * single["keys"].shape[0]
+    a, b = gpu_scores(grouped), gpu_scores(single)
+    assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
