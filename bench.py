@@ -31,6 +31,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -143,8 +144,11 @@ class ClockSampler:
         self.path = None
 
     def __enter__(self):
-        os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_gpu{self.index}.csv")
+        # The samples go to a temporary file (or BENCH_CLOCKS_DIR); their
+        # summary goes into the JSON line.
+        out_dir = os.environ.get("BENCH_CLOCKS_DIR") or tempfile.gettempdir()
+        os.makedirs(out_dir, exist_ok=True)
+        self.path = os.path.join(out_dir, f"clocks_gpu{self.index}_{os.getpid()}.csv")
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.index), f"--query-gpu={CLOCK_FIELDS}",
