@@ -164,6 +164,9 @@ def _indexer_args(q, w, keys, key_starts, lengths, score_starts, bias, scale):
         raise ValueError("key_starts, lengths and score_starts differ in size")
     if keys.numel() % INDEXER_DIM:
         raise ValueError(f"keys must be [n_keys, {INDEXER_DIM}]")
+    for t, name in ((q, "q"), (keys, "keys"), (w, "w")):
+        if t.numel() and t.data_ptr() % 16:
+            raise ValueError(f"{name} must start on a 16-byte boundary (the TMA and vector loads need it)")
     if bias is not None:
         _check(bias, "bias", torch.float32, dev)
         if bias.numel() != B:

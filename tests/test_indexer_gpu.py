@@ -238,3 +238,13 @@ def test_scores_do_not_depend_on_the_kernel_instance():
     assert 2 * grouped["keys"].shape[0] <= grouped["n_scores"] < 2 * single["keys"].shape[0]
     a, b = gpu_scores(grouped), gpu_scores(single)
     assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+
+
+def test_misaligned_inputs_are_refused_with_a_message():
+    c = make_case([100, 50], seed=14)
+    d = {k: (v.cuda() if isinstance(v, torch.Tensor) else v) for k, v in c.items()}
+    w_off = torch.empty(2 * H + 1, device="cuda")[1:].view(2, H)          # 4 bytes off a 16-byte boundary
+    w_off.copy_(d["w"])
+    with pytest.raises(ValueError, match="16-byte"):
+        pkg.indexer_scores(d["q"], w_off, d["keys"], d["key_starts"], d["lengths"], d["score_starts"],
+                           n_scores=c["n_scores"])
