@@ -890,7 +890,7 @@ __device__ __forceinline__ bool row_window_ok(const Params &p, int i, int64_t &l
 
 template <int THREADS>
 __device__ RowGroup assign_rows(const Params &p, uint32_t crank, uint32_t csize, uint32_t *scratch,
-                                uint32_t *work, uint32_t *slot)
+                                uint32_t *slot)
 {
     const int tid = threadIdx.x;
     const int B = p.B;   // at most 512 (the planner's cluster shapes hold fewer CTAs)
@@ -916,47 +916,56 @@ __device__ RowGroup assign_rows(const Params &p, uint32_t crank, uint32_t csize,
         by_rank[rank] = (uint32_t)i;
     }
     __syncthreads();
-    if (tid == 0) {
-        // The cluster's rows, their lengths and CTA counts (at most 16 each).
-        uint32_t *rows = work, *len = work + 16, *c = work + 32;
-        int m = 0;
-        for (int t0 = 0; t0 < B; t0 += 2 * G) {
-            const int ta = t0 + cid, tb = t0 + 2 * G - 1 - cid;
-            if (ta < B && m < 16) { rows[m] = by_rank[ta]; len[m] = eff[rows[m]]; ++m; }
-            if (tb < B && m < 16) { rows[m] = by_rank[tb]; len[m] = eff[rows[m]]; ++m; }
-        }
-        // Rows are listed in rank order, so the rows with work come first;
-        // a cluster holds at most csize of them (the planner guarantees it).
-        int mv = 0;
-        while (mv < m && mv < (int)csize && len[mv] > 0) ++mv;
-        int mine = -1;
-        uint32_t g0 = 0, gsize = 0;
-        if (mv > 0) {
-            // One CTA per row, then each spare CTA to the row with the
-            // largest slice (len / c; ties to the earlier row).
-            for (int i = 0; i < mv; ++i) c[i] = 1u;
-            for (uint32_t used = (uint32_t)mv; used < csize; ++used) {
-                int best = 0;
-                for (int i = 1; i < mv; ++i)
-                    if ((uint64_t)len[i] * c[best] > (uint64_t)len[best] * c[i]) best = i;
-                ++c[best];
-            }
-            uint32_t start = 0;
-            for (int i = 0; i < mv; ++i) {
-                if (crank >= start && crank < start + c[i]) {
-                    mine = (int)rows[i];
-                    g0 = start;
-                    gsize = c[i];
+    if (tid < 32) {
+        // The cluster's rows, one per lane of warp 0, in the order they are
+        // dealt: lane i holds rank t_i (the pair of block i / 2), and t_i
+        // grows with i, so the cluster's rows are lanes 0 .. m-1, and (ranks
+        // being sorted by length) the rows with work come first.  A cluster
+        // holds at most csize of them (the planner guarantees it).
+        const int lane = tid;
+        const int t0 = (lane >> 1) * 2 * G;
+        const int t = (lane & 1) ? t0 + 2 * G - 1 - cid : t0 + cid;
+        const bool exists = lane < 16 && t < B;
+        const uint32_t row_i = exists ? by_rank[t] : 0u;
+        const uint32_t len_i = exists ? eff[row_i] : 0u;
+        const int m = __popc(__ballot_sync(kFull, exists));
+        const uint32_t vb = __ballot_sync(kFull, exists && len_i > 0 && lane < (int)csize);
+        const int mv = __ffs(~vb) - 1;   // leading lanes with work
+        // One CTA per row, then each spare CTA to the row with the largest
+        // slice len / c (ties to the earlier row): a warp arg-max per spare.
+        // len < 2^24 and c <= 16, so the cross products fit 32 bits.
+        uint32_t c = lane < mv ? 1u : 0u;
+        const uint32_t lw = lane < mv ? len_i : 0u;
+        for (int used = mv; used < (int)csize && mv > 0; ++used) {
+            uint32_t bl = lw, bc = c > 0 ? c : 1u;
+            int bi = lane;
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) {
+                const uint32_t ol = __shfl_xor_sync(kFull, bl, o), oc = __shfl_xor_sync(kFull, bc, o);
+                const int oi = __shfl_xor_sync(kFull, bi, o);
+                if (ol * bc > bl * oc || (ol * bc == bl * oc && oi < bi)) {
+                    bl = ol;
+                    bc = oc;
+                    bi = oi;
                 }
-                start += c[i];
             }
+            if (lane == bi) ++c;
         }
-        slot[0] = (uint32_t)mine;
-        slot[1] = g0;
-        slot[2] = gsize;
-        // The cluster's first CTA pads the rows with nothing to select.
-        slot[3] = (uint32_t)(m - mv);
-        for (int i = mv; i < m; ++i) slot[4 + i - mv] = rows[i];
+        const uint32_t cs_incl = warp_incl_scan(c);
+        const uint32_t start = cs_incl - c;
+        const uint32_t own = __ballot_sync(kFull, c > 0 && crank >= start && crank < start + c);
+        const int owner = own ? __ffs(own) - 1 : 0;
+        const uint32_t o_row = __shfl_sync(kFull, row_i, owner);
+        const uint32_t o_g0 = __shfl_sync(kFull, start, owner);
+        const uint32_t o_gs = __shfl_sync(kFull, c, owner);
+        if (lane == 0) {
+            slot[0] = own ? o_row : 0xFFFFFFFFu;   // -1: no row with work for this CTA
+            slot[1] = own ? o_g0 : 0u;
+            slot[2] = own ? o_gs : 0u;
+            // The cluster's first CTA pads the rows with nothing to select.
+            slot[3] = (uint32_t)(m - mv);
+        }
+        if (lane >= mv && lane < m) slot[4 + lane - mv] = row_i;
     }
     __syncthreads();
     RowGroup g;
@@ -1994,7 +2003,7 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t crank = cluster_rank(), csize = cluster_size();
-    const RowGroup g = assign_rows<THREADS>(p, crank, csize, hist0, hist1, ctrl.scan);
+    const RowGroup g = assign_rows<THREADS>(p, crank, csize, hist0, ctrl.scan);
     if (g.row < 0) return;   // uniform over the cluster: nothing to select
     const int row = g.row;
     const uint32_t g0 = g.g0, gsize = g.gsize, grank = crank - g0;
