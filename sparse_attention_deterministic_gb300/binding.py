@@ -28,6 +28,23 @@ TOPK_STAT_ZERO_BOUND = 4
 MAX_K = 4096
 MAX_LEN = 1 << 24
 PAD_VALUE_BITS = 0xFF800000
+_STATUS_INVALID_ARG = 1   # TOPK_ERR_INVALID_ARG
+
+
+def _device(device) -> torch.device:
+    """The CUDA device named by `device` (an index, a string or a torch.device);
+    None or a bare "cuda" is the current one."""
+    d = torch.device("cuda", device) if isinstance(device, int) else torch.device(device or "cuda")
+    if d.type != "cuda":
+        raise ValueError(f"expected a CUDA device, got {d}")
+    return d if d.index is not None else torch.device("cuda", torch.cuda.current_device())
+
+
+def _check_k(k: int, B: int, what: str) -> None:
+    """The library's own k and B * k limits, checked before an output of B * k
+    entries is allocated for a call that would be refused."""
+    if not 1 <= int(k) <= MAX_K or B * int(k) >= 1 << 31:
+        raise TopkError(_STATUS_INVALID_ARG, f"{what} (k = {k}, B = {B})")
 
 
 def _stream_handle(device: torch.device, stream) -> int:
@@ -49,10 +66,28 @@ def _check(t: torch.Tensor, name: str, dtype, device=None):
         raise ValueError(f"{name} must be contiguous")
 
 
+def _outputs(out_idx, out_val, with_values: bool, B: int, k: int, dev, what: str):
+    """The selection's outputs: the caller's, checked to hold B * k entries,
+    or new ones."""
+    _check_k(k, B, what)
+    if out_idx is None:
+        out_idx = torch.empty((B, k), dtype=torch.int32, device=dev)
+    else:
+        _check(out_idx, "out_idx", torch.int32, dev)
+        if out_idx.numel() != B * k:
+            raise ValueError("out_idx must hold B * k entries")
+    if out_val is None and with_values:
+        out_val = torch.empty((B, k), dtype=torch.float32, device=dev)
+    elif out_val is not None:
+        _check(out_val, "out_val", torch.float32, dev)
+        if out_val.numel() != B * k:
+            raise ValueError("out_val must hold B * k entries")
+    return out_idx, out_val
+
+
 def init(device=None) -> None:
     """Prepare a device (outside stream capture); see topk_ragged_init."""
-    dev = torch.device("cuda", torch.cuda.current_device() if device is None else
-                       torch.device(device).index or 0)
+    dev = _device(device)
     with torch.cuda.device(dev):
         rc = lib().topk_ragged_init(dev.index)
     if rc != 0:
@@ -82,18 +117,12 @@ def topk_ragged(scores: torch.Tensor, row_starts: torch.Tensor, lengths: torch.T
     B = row_starts.numel()
     if lengths.numel() != B:
         raise ValueError(f"row_starts has {B} entries, lengths has {lengths.numel()}")
-    if out_idx is None:
-        out_idx = torch.empty((B, k), dtype=torch.int32, device=dev)
-    else:
-        _check(out_idx, "out_idx", torch.int32, dev)
-        if out_idx.numel() != B * k:
-            raise ValueError("out_idx must hold B * k entries")
-    if out_val is None and with_values:
-        out_val = torch.empty((B, k), dtype=torch.float32, device=dev)
-    elif out_val is not None:
-        _check(out_val, "out_val", torch.float32, dev)
-        if out_val.numel() != B * k:
-            raise ValueError("out_val must hold B * k entries")
+    if page_table is not None:
+        _check(page_table, "page_table", torch.int32, dev)
+        if page_table.dim() > 2 or (page_table.dim() == 2 and page_table.shape[0] != B):
+            raise ValueError("page_table must be [B, pages] (one row per query row) or [pages] (shared)")
+    out_idx, out_val = _outputs(out_idx, out_val, with_values, B, k, dev,
+                                "topk_ragged" if page_table is None else "topk_ragged_paged")
     common = (scores.data_ptr() if scores.numel() else None, scores.numel(),
               row_starts.data_ptr() if B else None, lengths.data_ptr() if B else None,
               B, int(k), int(offset_mode))
@@ -104,10 +133,7 @@ def topk_ragged(scores: torch.Tensor, row_starts: torch.Tensor, lengths: torch.T
             rc = lib().topk_ragged(*common, *tail)
             name = "topk_ragged"
         else:
-            _check(page_table, "page_table", torch.int32, dev)
             stride = page_table.shape[-1] if page_table.dim() == 2 else 0
-            if page_table.dim() == 2 and page_table.shape[0] != B:
-                raise ValueError("page_table must have one row per query row (or be 1-D)")
             rc = lib().topk_ragged_paged(*common, page_table.data_ptr() if page_table.numel() else None,
                                          stride, int(page_size), *tail)
             name = "topk_ragged_paged"
@@ -221,16 +247,7 @@ def topk_ragged_indexer(q: torch.Tensor, w: torch.Tensor, keys: torch.Tensor, ke
         scores = torch.zeros(int(n_scores), dtype=torch.float32, device=dev)
     else:
         _check(scores, "scores", torch.float32, dev)
-    if out_idx is None:
-        out_idx = torch.empty((B, k), dtype=torch.int32, device=dev)
-    else:
-        _check(out_idx, "out_idx", torch.int32, dev)
-        if out_idx.numel() != B * k:
-            raise ValueError("out_idx must hold B * k entries")
-    if out_val is None and with_values:
-        out_val = torch.empty((B, k), dtype=torch.float32, device=dev)
-    elif out_val is not None:
-        _check(out_val, "out_val", torch.float32, dev)
+    out_idx, out_val = _outputs(out_idx, out_val, with_values, B, k, dev, "topk_ragged_indexer")
     with torch.cuda.device(dev):
         rc = lib().topk_ragged_indexer(
             q.data_ptr() if B else None, w.data_ptr() if B else None,
@@ -246,8 +263,7 @@ def topk_ragged_indexer(q: torch.Tensor, w: torch.Tensor, keys: torch.Tensor, ke
 
 def device_status(device=None, stream=None) -> int:
     """Read and clear the device status word (synchronises the stream)."""
-    dev = torch.device("cuda", torch.cuda.current_device() if device is None else
-                       torch.device(device).index or 0)
+    dev = _device(device)
     v = ctypes.c_uint32(0)
     with torch.cuda.device(dev):
         rc = lib().topk_ragged_device_status(ctypes.byref(v), _stream_handle(dev, stream))
@@ -259,8 +275,7 @@ def device_status(device=None, stream=None) -> int:
 def launch_info(n_scores: int, B: int, k: int, device=None) -> dict:
     """How a call with (n_scores, B, k) is launched on the device: threads,
     cluster, grid, ..."""
-    dev = torch.device("cuda", torch.cuda.current_device() if device is None else
-                       torch.device(device).index or 0)
+    dev = _device(device)
     info = LaunchInfo()
     with torch.cuda.device(dev):
         rc = lib().topk_ragged_launch_info(int(n_scores), int(B), int(k), ctypes.byref(info))
