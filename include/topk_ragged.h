@@ -84,8 +84,8 @@ const char *topk_ragged_strerror(int status);
  * compute-capability 10.3 GPU, sets the kernels' shared-memory and cluster
  * attributes, and records the SM count used to size launches.  Idempotent and
  * thread-safe.  Must run outside stream capture; topk_ragged() calls it
- * itself on first use when the stream is not capturing.  Changes the calling
- * thread's current device to `device` and does not restore it.
+ * itself on first use when the stream is not capturing.  The calling
+ * thread's current device is the same on return as on entry.
  * Returns TOPK_OK, TOPK_ERR_UNSUPPORTED_DEVICE or TOPK_ERR_CUDA.
  */
 int topk_ragged_init(int device);
