@@ -8,7 +8,9 @@ batch of rows).  The default workload is the decode batch: 64 rows with
 lengths uniform in [4096, 131072], lightning-indexer scores, k = 2048.  The
 timed region replays the K launches from CUDA graphs over rotating input
 copies whose total exceeds 3x the L2 size, so every step reads cold scores
-from HBM.  Rank 0 prints one JSON line.
+from HBM.  Rank 0 prints one JSON line.  With the default workload the same
+run also times the other k = 2048 workload, the prefill chunk (16384 causal
+rows), by the same method, and reports it under "also" (--no-also skips it).
 
 --page-size P times the page-table transform (topk_ragged_paged) and
 --op stats the tie / plateau statistics op (topk_ragged_stats) on the same
@@ -63,6 +65,8 @@ def parse_args():
     p.add_argument("--e2e-steps", type=int, default=500)
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--no-also", action="store_true",
+                   help="with the default decode workload, skip the prefill record under 'also'")
     p.add_argument("--page-size", type=int, default=0,
                    help="write KV-cache slots through random per-row page tables of this "
                         "page size (topk_ragged_paged); 0: plain indices")
@@ -348,25 +352,19 @@ def run_reference(args, rank):
 # Our arm.
 # --------------------------------------------------------------------------- #
 
-def run_ours(args, rank, world, local):
+def measure(args, w, device, local, world, op="topk", page_size=0):
+    """Time one workload on this rank: cold-L2 graph replays of K launches
+    (the headline), warm L2, the end-to-end public call from pinned host
+    buffers, parity against the oracle and byte identity of the timed
+    launches.  Returns a dict of the measurements."""
+    import numpy as np
     import torch
 
+    import oracle
     import sparse_attention_deterministic_gb300 as pkg
-    import workloads as W
 
-    device = torch.device("cuda", local)
-    torch.cuda.set_device(device)
-    if world > 1:
-        import torch.distributed as dist
-        dist.init_process_group("gloo")
-    pkg.build()
-    pkg.init(device)
-
-    w = W.make(args.config, device=device)
     B, k, total = w.B, w.k, w.total_len()
-    stats = args.op == "stats"
-    if stats and args.page_size > 0:
-        raise SystemExit("--page-size applies to --op topk")
+    stats = op == "stats"
     out_cols = STATS_FIELDS if stats else k
     in_bytes = w.scores.numel() * 4 + 8 * B
     l2 = torch.cuda.get_device_properties(device).L2_cache_size
@@ -380,8 +378,8 @@ def run_ours(args, rank, world, local):
     # The page-table transform: random per-row page tables (the row-start
     # offset has no meaning there, so the mode keeps only its other bits).
     page_table, mode = None, w.offset_mode
-    if args.page_size > 0:
-        n_pages = -(-int(w.lengths.max()) // args.page_size)
+    if page_size > 0:
+        n_pages = -(-int(w.lengths.max()) // page_size)
         g = torch.Generator().manual_seed(1234)
         page_table = torch.stack([torch.randperm(4 * n_pages, generator=g)[:n_pages] for _ in range(B)]
                                  ).to(torch.int32).to(device)
@@ -392,15 +390,12 @@ def run_ours(args, rank, world, local):
             pkg.topk_ragged_stats(scores, starts, lengths, k, out=out, stream=s)
         else:
             pkg.topk_ragged(scores, starts, lengths, k, mode, out_idx=out, stream=s,
-                            page_table=page_table, page_size=max(args.page_size, 1))
+                            page_table=page_table, page_size=max(page_size, 1))
 
     def launch(i, s=stream):
         call(copies[i], w.row_starts, w.lengths, outs[i], s)
 
     # Parity guard: the timed configuration must match the oracle on this input.
-    import numpy as np
-
-    import oracle
     with torch.cuda.stream(stream):
         launch(0)
     stream.synchronize()
@@ -411,7 +406,7 @@ def run_ours(args, rank, world, local):
         ref, _, _ = oracle.topk_ragged(s_np, st_np, ln_np, k, mode,
                                        n_threads=len(os.sched_getaffinity(0)), with_values=False)
     if page_table is not None:
-        ref = oracle.paged_slots(ref, page_table.cpu().numpy(), args.page_size)
+        ref = oracle.paged_slots(ref, page_table.cpu().numpy(), page_size)
     parity = bool(np.array_equal(outs[0].cpu().numpy(), ref))
     if pkg.device_status(device) != 0:
         parity = False
@@ -459,7 +454,6 @@ def run_ours(args, rank, world, local):
             torch.distributed.barrier()
     ms = max_over_ranks(ev0.elapsed_time(ev1), world)
     ms_per_step = ms / args.steps
-    value = whole_job_rate(B, ms_per_step, world)
     # Every timed launch read an identical copy of the inputs, so their
     # outputs must agree byte for byte.
     torch.cuda.synchronize(device)
@@ -515,11 +509,72 @@ def run_ours(args, rank, world, local):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world) / args.e2e_steps
     e2e_parity = bool(np.array_equal(h_out.numpy(), ref))
 
-    if rank != 0:
-        return
     peak, peak_kind = hbm_peak()
     alg = algorithmic_bytes_stats(total, B) if stats else algorithmic_bytes(total, B, k)
     achieved = alg / (ms_per_step * 1e-3) / 1e9
+    return {
+        "B": B, "k": k, "total": total, "mode": mode, "info": info, "parity": parity,
+        "repeats_identical": repeats_identical, "n_copies": n_copies, "in_bytes": in_bytes, "l2": l2,
+        "ms_per_step": ms_per_step, "warm_ms": warm_ms, "e2e_ms": e2e_ms, "e2e_parity": e2e_parity,
+        "h2d": h_scores.numel() * 4 + 8 * B, "d2h": B * out_cols * 4, "alg": alg, "achieved": achieved,
+        "peak": peak, "peak_kind": peak_kind, "clocks": clocks.summary(),
+        "traffic": stored_traffic(w.name + (":stats" if stats else "")),
+    }
+
+
+def roofline_of(m):
+    return {"bound": "hbm", "achieved": m["achieved"], "peak": m["peak"], "unit": "GB/s",
+            "frac": m["achieved"] / m["peak"], "peak_kind": m["peak_kind"],
+            "frac_of_nominal": m["achieved"] / NOMINAL_HBM_GBS, "traffic": m["traffic"],
+            "algorithmic_bytes_per_launch": m["alg"]}
+
+
+def run_ours(args, rank, world, local):
+    import torch
+
+    import sparse_attention_deterministic_gb300 as pkg
+    import workloads as W
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("gloo")
+    pkg.build()
+    pkg.init(device)
+
+    stats = args.op == "stats"
+    if stats and args.page_size > 0:
+        raise SystemExit("--page-size applies to --op topk")
+    w = W.make(args.config, device=device)
+    m = measure(args, w, device, local, world, op=args.op, page_size=args.page_size)
+    # The second k = 2048 workload, prefill, in the same run and by the same
+    # method, beside the decode headline.
+    also = None
+    if args.config == "decode" and args.op == "topk" and args.page_size == 0 and not args.no_also:
+        wp = W.make("prefill", device=device)
+        mp = measure(args, wp, device, local, world)
+        also = {"prefill": {
+            "workload": "prefill", "B": mp["B"], "k": mp["k"], "sum_len": mp["total"],
+            "offset_mode": mp["mode"], "ms_per_step": mp["ms_per_step"],
+            "value": whole_job_rate(mp["B"], mp["ms_per_step"], world), "unit": "rows/s",
+            "elements_per_s": whole_job_rate(mp["total"], mp["ms_per_step"], world),
+            "achieved_gbs": mp["achieved"], "roofline": roofline_of(mp), "launch": mp["info"],
+            "parity_vs_oracle": mp["parity"], "timed_launches_identical": mp["repeats_identical"],
+            "warm_l2": {"ms_per_step": mp["warm_ms"], "achieved_gbs": mp["alg"] / (mp["warm_ms"] * 1e-3) / 1e9},
+            "e2e": {"value": whole_job_rate(mp["B"], mp["e2e_ms"], world), "unit": "rows/s",
+                    "h2d_bytes_per_step": mp["h2d"], "d2h_bytes_per_step": mp["d2h"],
+                    "ms_per_step": mp["e2e_ms"], "parity_vs_oracle": mp["e2e_parity"]},
+            "l2": f"{mp['n_copies']} rotating input copies ({mp['n_copies'] * mp['in_bytes'] / 1e6:.0f} MB"
+                  f" > 3x L2 {mp['l2'] / 1e6:.0f} MB): cold scores every step",
+            "gpu_launches": args.steps * mp["info"]["launches"],
+            "clocks": mp["clocks"],
+        }}
+
+    if rank != 0:
+        return
+    B, total = m["B"], m["total"]
+    ms_per_step = m["ms_per_step"]
     cpu = None
     if not args.no_cpu_baseline and world == 1:
         rps, eps, threads, desc = time_oracle(w.to("cpu"), args.cpu_seconds, op=args.op)
@@ -528,34 +583,32 @@ def run_ours(args, rank, world, local):
                "sample": desc, "elements_per_s": eps,
                "single_thread": {"value": rps1, "unit": "rows/s", "sample": desc1}}
     line = {
-        "metric": METRIC_STATS if stats else METRIC, "value": value, "unit": "rows/s", "n_gpus": world,
+        "metric": METRIC_STATS if stats else METRIC, "value": whole_job_rate(B, ms_per_step, world),
+        "unit": "rows/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "u32",
         "data": "synthetic",
-        "config": {"workload": w.name, "B": B, "k": k, "sum_len": total,
-                   "offset_mode": mode, "page_size": args.page_size, "op": args.op, "scores": "fp32",
-                   "l2": f"{n_copies} rotating input copies ({n_copies * in_bytes / 1e6:.0f} MB"
-                         f" > 3x L2 {l2 / 1e6:.0f} MB): cold scores every step",
+        "config": {"workload": args.config, "B": B, "k": m["k"], "sum_len": total,
+                   "offset_mode": m["mode"], "page_size": args.page_size, "op": args.op, "scores": "fp32",
+                   "l2": f"{m['n_copies']} rotating input copies ({m['n_copies'] * m['in_bytes'] / 1e6:.0f} MB"
+                         f" > 3x L2 {m['l2'] / 1e6:.0f} MB): cold scores every step",
                    "timing": "CUDA events around graph replays of K launches on one stream",
-                   "launch": info, "parity_vs_oracle": parity,
-                   "timed_launches_identical": repeats_identical},
+                   "launch": m["info"], "parity_vs_oracle": m["parity"],
+                   "timed_launches_identical": m["repeats_identical"]},
         "elements_per_s": whole_job_rate(total, ms_per_step, world),
-        "warm_l2": {"ms_per_step": warm_ms, "value": whole_job_rate(B, warm_ms, world), "unit": "rows/s",
-                    "achieved_gbs": alg / (warm_ms * 1e-3) / 1e9},
-        "achieved_gbs": achieved,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "peak_kind": peak_kind,
-                     "frac_of_nominal": achieved / NOMINAL_HBM_GBS,
-                     "traffic": stored_traffic(w.name + (":stats" if stats else "")),
-                     "algorithmic_bytes_per_launch": alg},
+        "warm_l2": {"ms_per_step": m["warm_ms"], "value": whole_job_rate(B, m["warm_ms"], world),
+                    "unit": "rows/s", "achieved_gbs": m["alg"] / (m["warm_ms"] * 1e-3) / 1e9},
+        "achieved_gbs": m["achieved"],
+        "roofline": roofline_of(m),
         "cpu_baseline": cpu,
-        "e2e": {"value": whole_job_rate(B, e2e_ms, world), "unit": "rows/s",
-                "h2d_bytes_per_step": h_scores.numel() * 4 + 8 * B,
-                "d2h_bytes_per_step": B * out_cols * 4, "ms_per_step": e2e_ms,
-                "parity_vs_oracle": e2e_parity},
-        "gpu_launches": args.steps * info["launches"],
-        "clocks": clocks.summary(),
+        "e2e": {"value": whole_job_rate(B, m["e2e_ms"], world), "unit": "rows/s",
+                "h2d_bytes_per_step": m["h2d"], "d2h_bytes_per_step": m["d2h"], "ms_per_step": m["e2e_ms"],
+                "parity_vs_oracle": m["e2e_parity"]},
+        "gpu_launches": args.steps * m["info"]["launches"],
+        "clocks": m["clocks"],
     }
+    if also is not None:
+        line["also"] = also
     print(json.dumps(line), flush=True)
 
 

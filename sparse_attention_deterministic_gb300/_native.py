@@ -49,7 +49,7 @@ def build(force: bool = False, verbose: bool = False) -> str:
     os.makedirs(BUILD_DIR, exist_ok=True)
     csrc = os.path.dirname(SRC)
     newest = max([os.path.getmtime(HEADER)] + [os.path.getmtime(os.path.join(csrc, f))
-                                                for f in os.listdir(csrc) if f.endswith((".cu", ".cuh"))])
+                                                for f in os.listdir(csrc) if f.endswith((".cu", ".cuh", ".h"))])
     if not force and os.path.exists(LIB_PATH) and os.path.getmtime(LIB_PATH) >= newest:
         return LIB_PATH
     tmp = f"{LIB_PATH}.tmp{os.getpid()}"

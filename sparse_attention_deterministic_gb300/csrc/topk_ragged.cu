@@ -56,11 +56,16 @@
 
 #include <mutex>
 
+#include "plan.h"
 #include "topk_ragged.h"
 
 namespace {
 
-constexpr int kBins = 2048;            // 11-bit digits (the last level uses 10 bits)
+using topk_plan::CCtrl;
+using topk_plan::Ctrl;
+using topk_plan::kBins;   // 11-bit digits (the last level uses 10 bits)
+using topk_plan::kShortQuads;
+using topk_plan::kShortScores;
 constexpr uint32_t kFull = 0xFFFFFFFFu;
 constexpr uint32_t kNegInfBits = 0xFF800000u;
 constexpr int kMaxDevices = 64;
@@ -86,28 +91,8 @@ struct Params {
     int32_t ahead;               // row kernel: L2 prefetch distance in rows (0: none)
 };
 
-// Per-CTA control block at the start of dynamic shared memory.
-struct __align__(16) Ctrl {
-    uint32_t sel_digit;  // result of the last threshold search
-    uint32_t sel_gt;     //   entries above the chosen bin (within the prefix)
-    uint32_t sel_cnt;    //   entries in the chosen bin
-    uint32_t sel_done;   //   1: the k-th key is +0.0 (plateau shortcut)
-    uint32_t zeros;      // count of exact +0.0 scores
-    uint32_t win_count;  // winner slots handed out
-    uint32_t kmax;       // the largest order key
-    uint32_t wmin;       // the smallest winner key
-    uint32_t warp_zeros[32];
-    uint32_t warp_ties[32];
-    uint32_t scan[36];
-    uint64_t scan64[32];
-    // Short-row path: per-warp partials (entries above +0.0, +0.0 count,
-    // smallest and largest non-zero key) and the bucket statistics.
-    uint32_t part_p[32], part_z[32], part_min[32], part_max[32];
-    uint32_t sq;         // sum of squared sizes of the buckets that are output
-    uint32_t npart;      // entries in those buckets
-    uint32_t tot_p;      // entries above +0.0
-    uint32_t tot_z;      // +0.0 entries
-};
+// Per-CTA control blocks (Ctrl, CCtrl) sit at the start of dynamic shared
+// memory; plan.h defines them beside the launch planner that sizes them.
 
 // ------------------------------------------------------------------------- //
 // Order key: fp32 bits -> uint32 whose unsigned order is the bitwise total
@@ -587,8 +572,6 @@ __device__ __forceinline__ void pad_out(int32_t *oi, float *ov, int from, int to
 // stay cheap (heavy ties off +0.0) or overflow the scratch, the function
 // returns false with shared memory released and the general path runs.
 // ------------------------------------------------------------------------- //
-constexpr int kShortQuads = 4;
-constexpr int kShortScores = 4 * kShortQuads * 256;   // scores the one-CTA short path holds
 constexpr int kShortBucketBits = 12;   // 2 * kBins buckets with 16-bit counters
 
 template <int THREADS>
@@ -1424,19 +1407,6 @@ __global__ void __launch_bounds__(THREADS, 5) topk_row_kernel(const Params p)
 // Every CTA of the cluster runs the same four cluster barriers whatever
 // its row needs.
 // ------------------------------------------------------------------------- //
-struct __align__(16) CCtrl {
-    uint64_t bar;          // completion of the slice's bulk copies
-    uint32_t zeros;        // this CTA's count of exact +0.0 keys
-    uint32_t win_local;    // entries in this CTA's candidate list
-    uint32_t wmin;         // smallest candidate key in this CTA's list
-    uint32_t wmax;         // largest candidate key in this CTA's list
-    uint32_t sel[4];       // threshold search result: digit, above, in bin
-    uint32_t tot[4];       // group totals: +0.0 count
-    uint32_t warp_zeros[32];
-    uint32_t warp_ties[32];
-    uint32_t scan[36];
-    uint64_t scan64[32];
-};
 
 // Sum of the group's histograms over this thread's BPT bins starting at lo.
 template <int THREADS>
@@ -2571,26 +2541,18 @@ __global__ void __launch_bounds__(THREADS) topk_stats_kernel(const float *scores
 // ------------------------------------------------------------------------- //
 typedef void (*KernelFn)(const Params);
 
-struct Variant {
-    KernelFn fn;
-    int threads;
-    bool cluster;
-};
-
-const Variant kVariants[] = {
-    {topk_row_kernel<256>, 256, false},
-    {topk_cluster_kernel<512>, 512, true},
-    {topk_cluster_kernel<1024>, 1024, true},
+// The top-k kernel of each planner variant (topk_plan::kRowKernel,
+// kCluster512, kCluster1024).
+const KernelFn kVariantFn[topk_plan::kVariants] = {
+    topk_row_kernel<256>,
+    topk_cluster_kernel<512>,
+    topk_cluster_kernel<1024>,
 };
 
 struct DeviceInfo {
     bool ready = false;
     int status = TOPK_OK;
-    int sm_count = 0;
-    int max_smem = 0;      // opt-in dynamic shared memory per block
-    int smem_per_sm = 0;   // shared memory per multiprocessor
-    // max_clusters[variant][C]: co-resident clusters of C CTAs (0 = not launchable)
-    int max_clusters[3][17] = {};
+    topk_plan::DeviceShape shape = {};
 };
 
 std::mutex g_mutex;
@@ -2610,98 +2572,11 @@ bool encode_bf16_rows(CUtensorMap *map, const void *base, uint64_t rows, uint32_
 }
 DeviceInfo g_devices[kMaxDevices];
 
-struct Plan {
-    const Variant *v;
-    int cluster;
-    int stage_cap;
-    int win_cap;
-    int off_win, off_keys, smem;
-    int grid;
-};
-
-int next_pow2(int x)
-{
-    int n = 1;
-    while (n < x) n <<= 1;
-    return n;
-}
-
-int header_bytes(bool cluster)
-{
-    return cluster ? (int)sizeof(CCtrl) + 2 * kBins * 4 : (int)sizeof(Ctrl) + kBins * 4;
-}
-
-// Candidate slots: the one-CTA kernel keeps the winners (fewer than k); the
-// cluster kernel's leader keeps up to twice k candidates, so that most rows
-// can be sorted after one or two histogram levels.
-int list_cap(bool cluster, int k)
-{
-    return cluster ? 2 * next_pow2(k) : next_pow2(k - 1 > 1 ? k - 1 : 1);
-}
-
-// Launch shape from the host arguments alone (row lengths live on the
-// device and are never read here).
-//   * B >= 4 x SMs: one 256-thread CTA per row, several CTAs per SM.
-//   * otherwise one resident wave of G clusters of CS CTAs, either
-//     1024-thread CTAs with all of an SM's shared memory or 512-thread CTAs
-//     two to an SM; the clusters share out the rows by length and each
-//     cluster deals its CTAs to its rows so that the largest slice is as
-//     small as possible (assign_rows).  Of the shapes that give every row a
-//     CTA, the planner takes the one whose typical row gets the most staging
-//     capacity, min(CS, G x CS / B) x scores staged per CTA, and on a tie the
-//     one with more CTAs.
-//   * batches too large for that wave fall back to one CTA per row.
-// Each CTA stages what shared memory allows and re-reads the rest of its
-// slice from L2.
-int stage_cap_for(int smem_budget, int off_keys)
-{
-    return ((smem_budget - off_keys) / 4) & ~127;
-}
+using topk_plan::Plan;
 
 Plan make_plan(int64_t n_scores, int32_t B, int32_t k, const DeviceInfo &dev)
 {
-    Plan pl{};
-    const int sms = dev.sm_count;
-    // The staged keys are read as 16-byte vectors: keep them 128-byte aligned
-    // whatever the winner array's size (k <= 2 gives a single 8-byte slot).
-    const int off_keys_cluster = (header_bytes(true) + list_cap(true, k) * 8 + 127) & ~127;
-    int vi = 0, cluster = 1, smem_budget = 0, grid = B;
-    // Short rows on average (the buffer holds at most kShortScores scores per
-    // row) go to the one-CTA-per-row kernel, whose short path ranks such a
-    // row in registers; clusters pay off for longer rows.
-    const bool short_rows = n_scores <= (int64_t)B * kShortScores;
-    if (B < 4 * sms && !short_rows) {
-        double best = 0.0;
-        for (int v = 2; v >= 1; --v) {
-            const int budget = v == 2 ? dev.max_smem : dev.smem_per_sm / 2 - 1024;
-            const int cap = stage_cap_for(budget, off_keys_cluster);
-            for (int cs = 2; cs <= 16; cs *= 2) {
-                int g = dev.max_clusters[v][cs];
-                if (v == 1) g = min(g, 2 * sms / cs);
-                if (g <= 0 || (int64_t)g * cs < B || cap <= 0) continue;
-                const double share = min((double)cs, (double)g * cs / B) * cap;
-                if (share > best * 1.0001 || (share > best * 0.9999 && g * cs > grid)) {
-                    best = share;
-                    vi = v;
-                    cluster = cs;
-                    smem_budget = budget;
-                    grid = g * cs;
-                }
-            }
-        }
-    }
-    pl.v = &kVariants[vi];
-    pl.cluster = cluster;
-    pl.win_cap = list_cap(pl.v->cluster, k);
-    pl.off_win = header_bytes(pl.v->cluster);
-    pl.off_keys = (pl.off_win + pl.win_cap * 8 + 127) & ~127;
-    int stage_cap = smem_budget > 0 ? stage_cap_for(smem_budget, pl.off_keys) : 4096 + 256;
-    // The staging area doubles as the sort's second buffer after compaction.
-    if (stage_cap < 2 * pl.win_cap) stage_cap = 2 * pl.win_cap;
-    pl.stage_cap = stage_cap;
-    pl.smem = pl.off_keys + stage_cap * 4;
-    pl.grid = grid;
-    return pl;
+    return topk_plan::make_plan(n_scores, B, k, dev.shape);
 }
 
 int init_locked(int device)
@@ -2721,19 +2596,20 @@ int init_locked(int device)
     }
     if (cudaSetDevice(device) != cudaSuccess) return TOPK_ERR_CUDA;
     int rc = TOPK_OK;
-    if (cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
-        cudaDeviceGetAttribute(&d.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess)
+    topk_plan::DeviceShape &sh = d.shape;
+    if (cudaDeviceGetAttribute(&sh.sm_count, cudaDevAttrMultiProcessorCount, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sh.max_smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, device) != cudaSuccess)
         rc = TOPK_ERR_CUDA;
     if (rc == TOPK_OK &&
-        cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device) != cudaSuccess)
+        cudaDeviceGetAttribute(&sh.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, device) != cudaSuccess)
         rc = TOPK_ERR_CUDA;
-    for (const Variant &v : kVariants) {
-        if (rc != TOPK_OK) break;
-        if (cudaFuncSetAttribute((const void *)v.fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 d.max_smem) != cudaSuccess)
+    for (int v = 0; v < topk_plan::kVariants && rc == TOPK_OK; ++v) {
+        if (cudaFuncSetAttribute((const void *)kVariantFn[v], cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 sh.max_smem) != cudaSuccess)
             rc = TOPK_ERR_CUDA;
-        if (v.cluster && cudaFuncSetAttribute((const void *)v.fn,
-                                              cudaFuncAttributeNonPortableClusterSizeAllowed, 1) != cudaSuccess)
+        if (v != topk_plan::kRowKernel &&
+            cudaFuncSetAttribute((const void *)kVariantFn[v], cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+                cudaSuccess)
             rc = TOPK_ERR_CUDA;
     }
     if (rc == TOPK_OK && cudaFuncSetAttribute((const void *)topk_stats_cluster_kernel<kStatsThreads>,
@@ -2758,13 +2634,12 @@ int init_locked(int device)
     }
     // Which cluster sizes each clustered variant can actually co-schedule
     // with the shared memory the planner gives it.
-    for (int vi = 1; vi < 3 && rc == TOPK_OK; ++vi) {
-        const Variant &v = kVariants[vi];
-        const int smem = vi == 2 ? d.max_smem : d.smem_per_sm / 2 - 1024;
+    for (int vi = topk_plan::kCluster512; vi < topk_plan::kVariants && rc == TOPK_OK; ++vi) {
+        const int smem = topk_plan::variant_budget(sh, vi);
         for (int c = 2; c <= 16; c *= 2) {
             cudaLaunchConfig_t cfg = {};
             cfg.gridDim = dim3((unsigned)(c * 8), 1, 1);
-            cfg.blockDim = dim3((unsigned)v.threads, 1, 1);
+            cfg.blockDim = dim3((unsigned)topk_plan::kVariantThreads[vi], 1, 1);
             cfg.dynamicSmemBytes = (size_t)smem;
             cudaLaunchAttribute attr[1];
             attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -2774,13 +2649,13 @@ int init_locked(int device)
             cfg.attrs = attr;
             cfg.numAttrs = 1;
             int n = 0;
-            if (cudaOccupancyMaxActiveClusters(&n, (const void *)v.fn, &cfg) != cudaSuccess) {
+            if (cudaOccupancyMaxActiveClusters(&n, (const void *)kVariantFn[vi], &cfg) != cudaSuccess) {
                 cudaGetLastError();
                 n = 0;
             }
-            d.max_clusters[vi][c] = n;
+            sh.max_clusters[vi][c] = n;
         }
-        d.max_clusters[vi][1] = 1;
+        sh.max_clusters[vi][1] = 1;
     }
     cudaSetDevice(prev);
     if (rc == TOPK_OK) {
@@ -2849,7 +2724,7 @@ int topk_ragged_launch_info(int64_t n_scores, int32_t B, int32_t k, topk_launch_
     int rc = ensure_init(device, true);
     if (rc != TOPK_OK) return rc;
     const Plan pl = make_plan(n_scores, B, k, g_devices[device]);
-    info->threads = pl.v->threads;
+    info->threads = topk_plan::kVariantThreads[pl.variant];
     info->cluster = pl.cluster;
     info->stage_cap = pl.stage_cap;
     info->smem_bytes = pl.smem;
@@ -2888,12 +2763,13 @@ static int launch(const float *scores, int64_t n_scores, const int32_t *row_star
     prm.page_table = page_table;
     prm.pt_stride = pt_stride;
     prm.page_size = page_size;
-    prm.ahead = pl.v->cluster ? 0 : g_devices[device].sm_count * 5;
+    const bool clustered = pl.variant != topk_plan::kRowKernel;
+    prm.ahead = clustered ? 0 : g_devices[device].shape.sm_count * topk_plan::kRowCtasPerSm;
     prm.page_shift = (page_size & (page_size - 1)) == 0 ? __builtin_ctz((unsigned)page_size) : -1;
 
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)pl.grid, 1, 1);
-    cfg.blockDim = dim3((unsigned)pl.v->threads, 1, 1);
+    cfg.blockDim = dim3((unsigned)topk_plan::kVariantThreads[pl.variant], 1, 1);
     cfg.dynamicSmemBytes = (size_t)pl.smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
@@ -2901,14 +2777,14 @@ static int launch(const float *scores, int64_t n_scores, const int32_t *row_star
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (pl.v->cluster) {
+    if (clustered) {
         attr[1].id = cudaLaunchAttributeClusterDimension;
         attr[1].val.clusterDim.x = (unsigned)pl.cluster;
         attr[1].val.clusterDim.y = 1;
         attr[1].val.clusterDim.z = 1;
         cfg.numAttrs = 2;
     }
-    if (cudaLaunchKernelEx(&cfg, pl.v->fn, prm) != cudaSuccess) {
+    if (cudaLaunchKernelEx(&cfg, kVariantFn[pl.variant], prm) != cudaSuccess) {
         cudaGetLastError();
         return TOPK_ERR_CUDA;
     }
@@ -2960,7 +2836,7 @@ int topk_ragged_stats(const float *scores, int64_t n_scores, const int32_t *row_
     // to 16 CTAs, so that the batch covers about two CTAs per SM and every
     // CTA keeps at least 16 K scores on average; otherwise one CTA per row.
     int cs = 1;
-    while (cs < 16 && (int64_t)B * cs * 2 <= 2LL * g_devices[device].sm_count &&
+    while (cs < 16 && (int64_t)B * cs * 2 <= 2LL * g_devices[device].shape.sm_count &&
            n_scores >= (int64_t)B * cs * 2 * 16384)
         cs *= 2;
     cudaLaunchConfig_t cfg = {};
@@ -3033,7 +2909,7 @@ int topk_ragged_indexer_scores(const uint16_t *q, const float *w, const float *b
     prm.B = B;
     prm.scale = scale;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)g_devices[device].sm_count, 1, 1);
+    cfg.gridDim = dim3((unsigned)g_devices[device].shape.sm_count, 1, 1);
     cfg.blockDim = dim3((unsigned)(grouped ? IxCfg<kIxGroup>::kThreads : IxCfg<1>::kThreads), 1, 1);
     cfg.dynamicSmemBytes = grouped ? IxCfg<kIxGroup>::kSmemBytes : IxCfg<1>::kSmemBytes;
     cfg.stream = st;

@@ -173,8 +173,8 @@ def test_planted_slip_is_caught(name):
 # Closed forms of the sglang page's tie-safety families: a plateau row of m
 # distinct positives and L - m exact zeros has, for m < k, its boundary on
 # the zero plateau with a tie set of L - m; a tie block of T copies of 1.0
-# placed so that k - T//2 distinct larger values sit above it has the
-# boundary 1.0 with tie T and above k - T//2.
+# with `above` distinct larger values, where the block straddles the k-th
+# place (above < k < above + T), has the boundary 1.0 with tie T.
 # --------------------------------------------------------------------------- #
 @pytest.mark.parametrize("m", [0, 1, 256, 1024, 2047])
 def test_plateau_family_closed_form(m):
@@ -193,6 +193,7 @@ def test_tie_block_family_closed_form(T):
     w = W.tie_block(3, L, k, T)
     s, st, ln = w.numpy()
     stats, _ = oracle.row_stats(s, st, ln, k)
-    above = max(0, k - T // 2)
+    above = w.info["above"]
+    assert max(0, k - T + 1) <= above < k
     for row in stats.tolist():
         assert row == [L, 0, 0x3F800000, T, above, HAS | STR]

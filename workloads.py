@@ -290,28 +290,42 @@ def _uniform(name, rows: torch.Tensor, k: int, offset_mode: int = 0, info=None) 
 
 
 def plateau(B: int, L: int, m: int, k: int, seed: int = 7) -> Workload:
-    """m distinct positives 0.5 + i*1e-3 at random positions, rest 0.0."""
+    """The plateau family: every row holds m distinct positive scores and
+    L - m exact zeros.  Positions come from one random ordering of the row
+    (argsort of uniform draws), and the positives are a random arrangement of
+    the integers 1..m, so they are distinct and exact in fp32."""
+    assert 0 <= m <= L < (1 << 24)
     g = _gen(seed, "cpu")
     rows = torch.zeros(B, L)
-    vals = 0.5 + torch.arange(m, dtype=torch.float32) * 1e-3
-    for b in range(B):
-        pos = torch.randperm(L, generator=g)[:m]
-        rows[b, pos] = vals[torch.randperm(m, generator=g)]
+    if m:
+        where = torch.rand(B, L, generator=g).argsort(dim=1)[:, :m]
+        vals = torch.rand(B, m, generator=g).argsort(dim=1).to(torch.float32) + 1.0
+        rows.scatter_(1, where, vals)
     return _uniform(f"plateau_m{m}", rows, k, info={"m": m})
 
 
 def tie_block(B: int, L: int, k: int, T: int, seed: int = 11) -> Workload:
-    """T entries exactly 1.0 straddling the boundary; max(0, k - T//2) distinct
-    values above (2.0 + i*1e-4) and distinct small values below."""
+    """The tie-block family: T copies of 1.0 that straddle the k-th boundary.
+    Per row, the number of larger scores `above` is drawn so that the
+    boundary falls strictly inside the block (max(0, k - T + 1) <= above
+    <= k - 1, so the selection takes part of the tie set); the larger scores
+    are distinct values in (1, 2] and the rest distinct values in (0, 1).
+    Every row of a call uses the same `above` (in ``info``)."""
+    assert 2 <= T and k <= 4096
     g = _gen(seed, "cpu")
-    above = max(0, k - T // 2)
+    lo = max(0, k - T + 1)
+    above = int(torch.randint(lo, k, (1,), generator=g).item())
+    below = L - above - T
+    assert below >= 0 and below < (1 << 18)
+    order = torch.rand(B, L, generator=g).argsort(dim=1)
+    # Ranks 0..L-1 of a random ordering: the first `above` places get the
+    # larger values, the next T the tie value, the rest the smaller ones.
+    vals = torch.empty(L)
+    vals[:above] = 1.0 + (torch.randperm(above, generator=g).to(torch.float32) + 1.0) * 2.0 ** -12
+    vals[above:above + T] = 1.0
+    vals[above + T:] = (torch.randperm(below, generator=g).to(torch.float32) + 1.0) * 2.0 ** -18
     rows = torch.empty(B, L)
-    for b in range(B):
-        pos = torch.randperm(L, generator=g)
-        rows[b, pos[:above]] = 2.0 + torch.arange(above, dtype=torch.float32) * 1e-4
-        rows[b, pos[above:above + T]] = 1.0
-        nb = L - above - T
-        rows[b, pos[above + T:]] = 0.01 + torch.arange(nb, dtype=torch.float32) * 1e-7
+    rows.scatter_(1, order, vals.expand(B, L).contiguous())
     return _uniform(f"tie_T{T}", rows, k, info={"T": T, "above": above})
 
 
