@@ -50,7 +50,9 @@ typedef enum {
     TOPK_ERR_INVALID_ARG = 1,        /* an argument outside the contract below  */
     TOPK_ERR_NOT_INITIALIZED = 2,    /* called under stream capture before init */
     TOPK_ERR_UNSUPPORTED_DEVICE = 3, /* not a compute-capability 10.3 device    */
-    TOPK_ERR_CUDA = 4                /* a CUDA runtime call or launch failed    */
+    TOPK_ERR_CUDA = 4,               /* a CUDA runtime call or launch failed    */
+    TOPK_ERR_SCRATCH_TOO_SMALL = 5   /* n_scores beyond the library's fixed
+                                        score array (topk_ragged_indexer_static) */
 } topk_status;
 
 /* offset_mode: TOPK_OFFSET_ROW_LOCAL or TOPK_OFFSET_ROW_START, optionally
@@ -231,6 +233,48 @@ int topk_ragged_indexer(const uint16_t *q, const float *w, const float *bias, co
                         int64_t n_keys, const int32_t *key_starts, const int32_t *lengths,
                         const int32_t *score_starts, int32_t B, float scale, float *scores, int64_t n_scores,
                         int32_t k, int32_t flags, int32_t *out_idx, float *out_val, void *stream);
+
+/*
+ * topk_ragged_indexer for callers that cannot allocate device memory.  The
+ * chain's intermediate scores go to a score array that the library itself
+ * holds, not to a caller buffer, so the caller provides only the inputs and
+ * the outputs.  Callers that cannot allocate include code that runs inside
+ * a framework which reserves the device memory for its own allocator or
+ * cache up front (a plugin has no budget left to call cudaMalloc with, and
+ * a call would fail or fragment the pool), and code on a latency-critical
+ * path where cudaMalloc would synchronize the device or is not allowed at
+ * all (cudaMalloc is refused while a stream is captured in the global mode).
+ * The sources this library follows have no counterpart of this entry point;
+ * it is an addition of this library.
+ *
+ * The array holds TOPK_RAGGED_STATIC_SCORES fp32 scores (32 MiB).  Every GPU
+ * on which the library is loaded keeps it until the process exits.
+ * score_starts and n_scores lay the rows' score windows out inside it as
+ * they would inside a caller buffer: each window inside [0, n_scores), no
+ * two rows sharing a window.  0 <= n_scores <= TOPK_RAGGED_STATIC_SCORES;
+ * a larger n_scores returns TOPK_ERR_SCRATCH_TOO_SMALL and launches nothing.
+ *
+ * All calls on a device share the array, and each leaves its scores in it.
+ * Nothing in it has to start at zero: the score kernel writes every entry of
+ * a row's window before the selection reads it, and entries outside the
+ * windows are never read.  Calls whose work overlaps on the GPU (two
+ * streams, or two host threads, with nothing ordering them) race on the
+ * array and can read each other's scores: order them on one stream or with
+ * events.
+ *
+ * The first call on a device looks up the array's device address, with that
+ * device current, and keeps it for the later calls.  Make that first call
+ * outside stream capture: a first call under capture returns
+ * TOPK_ERR_NOT_INITIALIZED and launches nothing.  Everything else -- the
+ * arguments, the two launches on `stream`, the outputs, the device status
+ * bits and the return codes -- is as for topk_ragged_indexer.  The call
+ * allocates nothing.
+ */
+#define TOPK_RAGGED_STATIC_SCORES (1 << 23)
+int topk_ragged_indexer_static(const uint16_t *q, const float *w, const float *bias, const uint16_t *keys,
+                               int64_t n_keys, const int32_t *key_starts, const int32_t *lengths,
+                               const int32_t *score_starts, int32_t B, float scale, int64_t n_scores,
+                               int32_t k, int32_t flags, int32_t *out_idx, float *out_val, void *stream);
 
 /*
  * Reads the current device's status word (an OR of TOPK_DEV_* bits from all

@@ -29,6 +29,7 @@ EXPORTS = (
     "topk_ragged_stats",
     "topk_ragged_indexer_scores",
     "topk_ragged_indexer",
+    "topk_ragged_indexer_static",
     "topk_ragged_device_status",
     "topk_ragged_launch_info",
 )
@@ -109,6 +110,9 @@ def lib() -> ctypes.CDLL:
         so.topk_ragged_indexer_scores.restype = ctypes.c_int
         so.topk_ragged_indexer.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, i32, f32, vp, i64, i32, i32, vp, vp, vp]
         so.topk_ragged_indexer.restype = ctypes.c_int
+        so.topk_ragged_indexer_static.argtypes = [vp, vp, vp, vp, i64, vp, vp, vp, i32, f32, i64, i32, i32, vp, vp,
+                                                  vp]
+        so.topk_ragged_indexer_static.restype = ctypes.c_int
         so.topk_ragged_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_void_p]
         so.topk_ragged_device_status.restype = ctypes.c_int
         so.topk_ragged_launch_info.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,

@@ -261,6 +261,34 @@ def topk_ragged_indexer(q: torch.Tensor, w: torch.Tensor, keys: torch.Tensor, ke
     return out_idx, out_val, scores
 
 
+STATIC_SCORES = 1 << 23   # TOPK_RAGGED_STATIC_SCORES: scores the library's own array holds
+
+
+def topk_ragged_indexer_static(q: torch.Tensor, w: torch.Tensor, keys: torch.Tensor, key_starts: torch.Tensor,
+                               lengths: torch.Tensor, score_starts: torch.Tensor, n_scores: int, k: int = 2048,
+                               flags: int = 0, scale: float | None = None, bias: torch.Tensor | None = None,
+                               out_idx: torch.Tensor | None = None, out_val: torch.Tensor | None = None,
+                               with_values: bool = False, stream=None):
+    """The indexer chain with its scores in the library's own fixed array
+    (topk_ragged_indexer_static), for callers that cannot allocate device
+    memory: such a caller passes out_idx (and out_val) and nothing is
+    allocated; n_scores (at most STATIC_SCORES) bounds the score windows that
+    score_starts lays out in the array.  Returns (out_idx, out_val or None)."""
+    dev, B, scale = _indexer_args(q, w, keys, key_starts, lengths, score_starts, bias, scale)
+    out_idx, out_val = _outputs(out_idx, out_val, with_values, B, k, dev, "topk_ragged_indexer_static")
+    with torch.cuda.device(dev):
+        rc = lib().topk_ragged_indexer_static(
+            q.data_ptr() if B else None, w.data_ptr() if B else None,
+            bias.data_ptr() if (bias is not None and B) else None, keys.data_ptr() if keys.numel() else None,
+            keys.numel() // INDEXER_DIM, key_starts.data_ptr() if B else None, lengths.data_ptr() if B else None,
+            score_starts.data_ptr() if B else None, B, scale, int(n_scores), int(k), int(flags),
+            out_idx.data_ptr() if B else None, out_val.data_ptr() if (out_val is not None and B) else None,
+            _stream_handle(dev, stream))
+    if rc != 0:
+        raise TopkError(rc, "topk_ragged_indexer_static")
+    return out_idx, out_val
+
+
 def device_status(device=None, stream=None) -> int:
     """Read and clear the device status word (synchronises the stream)."""
     dev = _device(device)

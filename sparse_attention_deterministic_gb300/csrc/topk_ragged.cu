@@ -2536,6 +2536,12 @@ __global__ void __launch_bounds__(THREADS) topk_stats_kernel(const float *scores
 
 #include "indexer_scores.cuh"
 
+// Score array of topk_ragged_indexer_static: the chain's intermediate scores
+// for callers that cannot allocate device memory.  The host passes its
+// device address (looked up once per device) to the same two launches that
+// topk_ragged_indexer makes; no kernel names it directly.
+static __device__ __align__(256) float g_static_scores[TOPK_RAGGED_STATIC_SCORES];
+
 // ------------------------------------------------------------------------- //
 // Host side.
 // ------------------------------------------------------------------------- //
@@ -2571,6 +2577,9 @@ bool encode_bf16_rows(CUtensorMap *map, const void *base, uint64_t rows, uint32_
                           CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 DeviceInfo g_devices[kMaxDevices];
+// Device address of g_static_scores on each device (null until the first
+// topk_ragged_indexer_static call there looks it up).
+float *g_static_scores_addr[kMaxDevices] = {};
 
 using topk_plan::Plan;
 
@@ -2690,6 +2699,8 @@ const char *topk_ragged_strerror(int status)
     case TOPK_ERR_NOT_INITIALIZED: return "device not initialized (call topk_ragged_init outside stream capture)";
     case TOPK_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3)";
     case TOPK_ERR_CUDA: return "CUDA runtime error";
+    case TOPK_ERR_SCRATCH_TOO_SMALL:
+        return "n_scores exceeds the library's fixed score array (TOPK_RAGGED_STATIC_SCORES)";
     default: return "unknown status";
     }
 }
@@ -2939,6 +2950,39 @@ int topk_ragged_indexer(const uint16_t *q, const float *w, const float *bias, co
                                     n_scores, stream);
     if (rc != TOPK_OK) return rc;
     return topk_ragged(scores, n_scores, score_starts, lengths, B, k, flags, out_idx, out_val, stream);
+}
+
+int topk_ragged_indexer_static(const uint16_t *q, const float *w, const float *bias, const uint16_t *keys,
+                               int64_t n_keys, const int32_t *key_starts, const int32_t *lengths,
+                               const int32_t *score_starts, int32_t B, float scale, int64_t n_scores, int32_t k,
+                               int32_t flags, int32_t *out_idx, float *out_val, void *stream)
+{
+    if (n_scores > (int64_t)TOPK_RAGGED_STATIC_SCORES) return TOPK_ERR_SCRATCH_TOO_SMALL;
+    if (n_scores < 0 || k < 1 || k > TOPK_RAGGED_MAX_K || B < 0 || (flags & ~TOPK_EXCLUDE_NEG_INF) != 0)
+        return TOPK_ERR_INVALID_ARG;
+    if (B == 0) return TOPK_OK;
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return TOPK_ERR_CUDA;
+    if (device < 0 || device >= kMaxDevices) return TOPK_ERR_UNSUPPORTED_DEVICE;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing((cudaStream_t)stream, &cap) != cudaSuccess) return TOPK_ERR_CUDA;
+    float *scratch = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        scratch = g_static_scores_addr[device];
+        if (!scratch) {
+            if (cap != cudaStreamCaptureStatusNone) return TOPK_ERR_NOT_INITIALIZED;
+            // Set-up, once per device, with that device current: in host code
+            // g_static_scores names a host-side stand-in, not device memory.
+            if (cudaGetSymbolAddress((void **)&scratch, g_static_scores) != cudaSuccess || !scratch) {
+                cudaGetLastError();
+                return TOPK_ERR_CUDA;
+            }
+            g_static_scores_addr[device] = scratch;
+        }
+    }
+    return topk_ragged_indexer(q, w, bias, keys, n_keys, key_starts, lengths, score_starts, B, scale, scratch,
+                               n_scores, k, flags, out_idx, out_val, stream);
 }
 
 int topk_ragged_device_status(uint32_t *host_out, void *stream)
