@@ -59,6 +59,13 @@ struct alignas(16) CCtrl {
     uint32_t warp_ties[32];
     uint32_t scan[36];
     uint64_t scan64[32];
+    // Sampled path: the sample's largest key, this CTA's candidate-list
+    // overflow, the cluster's fallback flag (set remotely by any CTA whose
+    // row group falls back), the largest fine bin of the group, and the
+    // range of this CTA's share of the group's candidates in its buffer.
+    uint32_t smax, overflow, cl_fb, maxbin;
+    uint32_t loc_begin, loc_end, gz_before, pad0;
+    uint32_t gcnt[16];     // candidate-list lengths of the group's CTAs
 };
 
 // Kernel variants: the one-CTA-per-row kernel and the cluster kernel at 512

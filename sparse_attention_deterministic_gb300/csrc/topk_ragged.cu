@@ -1956,6 +1956,255 @@ __device__ __forceinline__ void compact(bool staged, CCtrl &ctrl, const Slice &s
                                              idx_offset, oi, ov, excl);
 }
 
+// ------------------------------------------------------------------------- //
+// Sampled path of the cluster kernel.
+//
+// Before the row's scores land in shared memory, every CTA of the row's
+// group reads the same deterministic sample of the row (the whole row when
+// L <= 4096, else 128 runs of 32 consecutive scores spread evenly over it)
+// and takes from it a lower bound
+// `lo` that, with overwhelming probability, lies at or below the k-th key:
+// the sample's m-th largest key rounded down to its 11-bit digit, where m is
+// the expected number of sampled entries above the k-th key plus four
+// standard deviations and 8 (m = k exactly when the sample is the whole
+// row).  One pass over the staged slice then keeps only the keys >= lo: they
+// are counted in a fine histogram of kFineBins bins over [lo, ...) and
+// appended to the CTA's candidate list as unique composites.  After one
+// cluster barrier every CTA of the group sums the group's fine histograms,
+// and the exclusive counts from the top give every fine bin its first output
+// place.  Each CTA then takes the bins whose first place falls in its share
+// of the output, gathers their members from the group's lists, ranks each
+// member inside its bin (composites are unique) and writes it at its place.
+// When the bound lies on or below the +0.0 key (a row whose k-th key may be
+// on the ReLU plateau) the candidates are the positive keys and the +0.0
+// entries are counted per warp: if the positives are fewer than k, the k-th
+// key is +0.0 and the first k - |positives| of them in index order follow.
+//
+// Every decision is taken from exact integer counts that all CTAs of the
+// group hold alike.  When a check fails (the bound was above the k-th key, a
+// list overflowed, a bin holds too many members to rank cheaply, or the k-th
+// key is below +0.0) the group falls back to the full radix select below,
+// on the same staged slice, so the result is the same either way.
+// ------------------------------------------------------------------------- //
+constexpr int kSample = 4096;       // scores of a row's sample
+constexpr int kFineBins = 1024;     // bins of the candidates' histogram
+constexpr uint32_t kMaxFineBin = 256;   // members a fine bin may hold on the sampled path
+
+// Fine bin of a candidate key e: bins of 2^sh keys from lo (the smallest
+// sampled candidate key); keys below lo share bin 0, keys past the last bin
+// share it.
+__device__ __forceinline__ uint32_t fine_bin(uint32_t e, uint32_t lo, uint32_t sh)
+{
+    if (e < lo) return 0u;
+    const uint32_t f = (e - lo) >> sh;
+    return f < (uint32_t)kFineBins ? f : (uint32_t)kFineBins - 1u;
+}
+
+// A full quad of the slice as keys: staged quads hold raw score bits.
+__device__ __forceinline__ uint4 raw_body_keys(const Slice &s, const uint4 *raw4, int q)
+{
+    if (q < s.sq) return to_keys(raw4[q]);
+    const float4 f = __ldg(reinterpret_cast<const float4 *>(s.gptr) + q);
+    return make_uint4(order_key(__float_as_uint(f.x)), order_key(__float_as_uint(f.y)),
+                      order_key(__float_as_uint(f.z)), order_key(__float_as_uint(f.w)));
+}
+
+// A partial (head or tail) quad as keys, with its valid slots in m.
+__device__ __forceinline__ uint4 raw_partial_keys(const Slice &s, const uint4 *raw4, int q, uint32_t &m)
+{
+    if (q < s.sq) {
+        m = quad_mask(s, q);
+        return to_keys(raw4[q]);
+    }
+    return load_quad_global(s, q, m);
+}
+
+// A full quad of the slice as raw score bits (staged, or read where it lies).
+__device__ __forceinline__ uint4 raw_body_quad(const Slice &s, const uint4 *raw4, int q)
+{
+    if (q < s.sq) return raw4[q];
+    const float4 f = __ldg(reinterpret_cast<const float4 *>(s.gptr) + q);
+    return make_uint4(__float_as_uint(f.x), __float_as_uint(f.y), __float_as_uint(f.z), __float_as_uint(f.w));
+}
+
+__device__ __forceinline__ int32_t quad_smax(const uint4 &r)
+{
+    return max(max((int32_t)r.x, (int32_t)r.y), max((int32_t)r.z, (int32_t)r.w));
+}
+
+// The pass over the slice: keys >= lo go to the fine histogram and to the
+// candidate list (slots from one shared-memory atomic per warp round; a
+// slot past wcap sets ctrl.overflow); with PLATEAU the +0.0 entries are
+// counted per warp in index order (ctrl.warp_zeros) and in all (ctrl.zeros).
+// lo is above the +0.0 key, so key >= lo holds exactly when the raw bits,
+// read as a signed integer, are >= lo_raw = lo - 0x80000000 (every negative
+// pattern is below every non-negative one): the scan compares raw bits and
+// only candidates are turned into keys.
+template <int THREADS, bool PLATEAU>
+__device__ void sampled_pass(CCtrl &ctrl, const Slice &s, const uint32_t *raw, const Parts &pt, uint32_t *fhist,
+                             uint64_t *win, uint32_t wcap, uint32_t lo, uint32_t f_lo, uint32_t sh)
+{
+    constexpr int U = kPassQuads;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint4 *raw4 = reinterpret_cast<const uint4 *>(raw);
+    const int32_t lo_raw = (int32_t)(lo - 0x80000000u);
+    uint32_t zeros = 0;
+    bool over = false;
+    auto put = [&](uint32_t u, int32_t j, uint32_t slot) {
+        const uint32_t e = order_key(u);
+        atomicAdd(&fhist[fine_bin(e, f_lo, sh)], 1u);
+        if (slot < wcap) win[slot] = ((uint64_t)e << 32) | (uint64_t)(~(uint32_t)j);
+        else over = true;
+    };
+    auto partial = [&](int q) {
+        uint32_t m;
+        uint4 r;
+        if (q < s.sq) {
+            m = quad_mask(s, q);
+            r = raw4[q];
+        } else {
+            m = quad_mask(s, q);
+            uint32_t e[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) e[i] = ((m >> i) & 1u) ? __float_as_uint(__ldg(s.gptr + 4 * q + i)) : 0u;
+            r = make_uint4(e[0], e[1], e[2], e[3]);
+        }
+        const uint32_t u4[4] = {r.x, r.y, r.z, r.w};
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (!((m >> i) & 1u)) continue;
+            if (PLATEAU) zeros += u4[i] == 0u;
+            if ((int32_t)u4[i] >= lo_raw) put(u4[i], s.jbase + 4 * q + i, atomicAdd(&ctrl.win_local, 1u));
+        }
+    };
+    if (lane == 0 && pt.head >= 0) partial(pt.head);
+    for (int qb = pt.q0; qb < pt.q1; qb += 32 * U) {
+        uint4 rr[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int q = qb + u * 32 + lane;
+            // Quads past the run read as -1 (below every bound, never +0.0).
+            rr[u] = q < pt.q1 ? raw_body_quad(s, raw4, q) : make_uint4(kFull, kFull, kFull, kFull);
+        }
+        uint32_t cm = 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            if (PLATEAU)
+                zeros += (uint32_t)(rr[u].x == 0u) + (uint32_t)(rr[u].y == 0u) + (uint32_t)(rr[u].z == 0u) +
+                         (uint32_t)(rr[u].w == 0u);
+            if (quad_smax(rr[u]) >= lo_raw) {
+                cm |= ((uint32_t)((int32_t)rr[u].x >= lo_raw) | (uint32_t)((int32_t)rr[u].y >= lo_raw) << 1 |
+                       (uint32_t)((int32_t)rr[u].z >= lo_raw) << 2 | (uint32_t)((int32_t)rr[u].w >= lo_raw) << 3)
+                      << (4 * u);
+            }
+        }
+        if (!__any_sync(kFull, cm != 0)) continue;
+        const uint32_t cnt = (uint32_t)__popc(cm);
+        const uint32_t ci = warp_incl_scan(cnt);
+        uint32_t base = 0;
+        if (lane == 31) base = atomicAdd(&ctrl.win_local, ci);
+        uint32_t slot = __shfl_sync(kFull, base, 31) + ci - cnt;
+        // One step per candidate of this lane (a few per round), not one
+        // per slot of the round.
+        while (cm) {
+            const int b = __ffs(cm) - 1;
+            cm &= cm - 1u;
+            const int u = b >> 2, i = b & 3;
+            const uint4 r = u == 0 ? rr[0] : rr[U - 1];
+            const uint32_t v = i == 0 ? r.x : i == 1 ? r.y : i == 2 ? r.z : r.w;
+            put(v, s.jbase + 4 * (qb + u * 32 + lane) + i, slot++);
+        }
+    }
+    if (lane == 0 && pt.tail >= 0) partial(pt.tail);
+    if (over) atomicOr(&ctrl.overflow, 1u);
+    if (PLATEAU) {
+        zeros = __reduce_add_sync(kFull, zeros);
+        if (lane == 0) {
+            ctrl.warp_zeros[warp] = zeros;
+            if (zeros) atomicAdd(&ctrl.zeros, zeros);
+        }
+    }
+}
+
+// The +0.0 entries of the slice in index order take output places
+// n_gt + ordinal for ordinals below r, the ordinals counting from
+// tie_base (the group's +0.0 entries before this CTA).  Walks the same
+// per-warp parts as sampled_pass, whose per-warp counts give each warp its
+// first ordinal.
+template <int THREADS>
+__device__ void write_zero_ties(CCtrl &ctrl, const Slice &s, const uint32_t *raw, const Parts &pt, uint32_t tie_base,
+                                uint32_t r, uint32_t n_gt, uint32_t k_eff, int64_t idx_offset, int32_t *oi, float *ov,
+                                bool excl)
+{
+    constexpr int NW = THREADS / 32;
+    constexpr int U = kPassQuads;
+    constexpr uint32_t kZ = 0x80000000u;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint4 *raw4 = reinterpret_cast<const uint4 *>(raw);
+    if (warp == 0) {
+        const uint32_t z = lane < NW ? ctrl.warp_zeros[lane] : 0u;
+        const uint32_t zi = warp_incl_scan(z);
+        if (lane < NW) ctrl.warp_ties[lane] = zi - z;
+    }
+    __syncthreads();
+    uint32_t tbase = tie_base + ctrl.warp_ties[warp];
+    if (ctrl.warp_zeros[warp] == 0 || tbase >= r) return;   // warp-uniform
+    auto put_tie = [&](int32_t j, uint32_t ord) {
+        if (ord < r && n_gt + ord < k_eff) put_out(oi, ov, n_gt + ord, idx_offset, j, kZ, excl);
+    };
+    auto partial = [&](int q) {
+        uint32_t t = 0;
+        if (lane == 0) {
+            uint32_t m;
+            const uint4 kk = raw_partial_keys(s, raw4, q, m);
+            const uint32_t e[4] = {kk.x, kk.y, kk.z, kk.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if (((m >> i) & 1u) && e[i] == kZ) put_tie(s.jbase + 4 * q + i, tbase + t++);
+        }
+        tbase += __shfl_sync(kFull, t, 0);
+    };
+    if (pt.head >= 0) partial(pt.head);
+    for (int qb = pt.q0; qb < pt.q1 && tbase < r; qb += 32 * U) {
+        uint4 kk[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int q = qb + u * 32 + lane;
+            kk[u] = q < pt.q1 ? raw_body_keys(s, raw4, q) : make_uint4(0, 0, 0, 0);
+        }
+        uint32_t tm = 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            tm |= ((uint32_t)(kk[u].x == kZ) | (uint32_t)(kk[u].y == kZ) << 1 | (uint32_t)(kk[u].z == kZ) << 2 |
+                   (uint32_t)(kk[u].w == kZ) << 3)
+                  << (4 * u);
+        if (!__any_sync(kFull, tm != 0)) continue;
+        // Index order inside a round: quad u, then lane, then slot; counts
+        // per u packed a byte each (at most 128) into one warp scan.
+        uint32_t packed = 0;
+#pragma unroll
+        for (int u = 0; u < U; ++u) packed |= (uint32_t)__popc((tm >> (4 * u)) & 0xFu) << (8 * u);
+        const uint32_t ti = warp_incl_scan(packed);
+        const uint32_t ttot = __shfl_sync(kFull, ti, 31), tex = ti - packed;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            uint32_t ord = tbase + ((tex >> (8 * u)) & 0xFFu);
+            const int32_t j0 = s.jbase + 4 * (qb + u * 32 + lane);
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                if ((tm >> (4 * u + i)) & 1u) put_tie(j0 + i, ord++);
+            tbase += (ttot >> (8 * u)) & 0xFFu;
+        }
+    }
+    if (pt.tail >= 0 && tbase < r) partial(pt.tail);
+}
+
+// Remote store into the shared memory of cluster CTA `rank`.
+__device__ __forceinline__ void dsmem_st(uint32_t addr, uint32_t v)
+{
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+
 template <int THREADS>
 __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kernel(const Params p)
 {
@@ -2018,8 +2267,25 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
     const Parts ptm = slice_parts<THREADS>(s, warp);   // masked parts (key-0 ranges)
     const uint32_t n_sentinel = (uint32_t)(4 * s.nq - (s.end - s.off0));
 
-    // ---- 1. bulk copies of the staged body; the partial head and tail
-    //         quads are read with plain loads ------------------------------- //
+    // ---- 1. the row's sample, then the bulk copies (TMA) of the staged
+    //         body; the sample and the partial head and tail quads are
+    //         read with plain loads into registers, the sample first so
+    //         that it is not queued behind the copies ------------------- //
+    // The sample: the whole row when L <= kSample, else 128 runs of 32
+    // consecutive scores spread evenly over the row (run t starts at
+    // t * (L - 32) / 127), so that it costs a few cache lines per row rather
+    // than a read of most of the row's DRAM bursts.  The same in every CTA
+    // of the group (raw bits; keys after the barrier).
+    constexpr int SPT = kSample / THREADS;
+    static_assert(kPassQuads == 2, "the append step below reads the round's two quads");
+    const uint32_t S = (uint32_t)(L < kSample ? L : kSample);
+    uint32_t skey[SPT];
+#pragma unroll
+    for (int u = 0; u < SPT; ++u) {
+        const uint32_t t = (uint32_t)tid + (uint32_t)(u * THREADS);
+        const uint32_t j = L <= kSample ? t : (t >> 5) * (uint32_t)(L - 32) / 127u + (t & 31u);
+        skey[u] = t < S ? __float_as_uint(__ldg(p.scores + rs + j)) : 0u;
+    }
     const int bq_end = s.bq1 < s.sq ? s.bq1 : s.sq;
     if (tid == 0) {
         mbar_init(&ctrl.bar, 1);
@@ -2030,16 +2296,16 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
                       reinterpret_cast<const unsigned char *>(s.gptr + 4 * s.bq0) + off,
                       bytes - off < kChunk ? bytes - off : kChunk, &ctrl.bar);
     }
-    {
-        // Staged quads outside the body: at most one head and one tail quad.
-        const int q = tid < 1 ? 0 : s.nq - 1;
-        if (tid < 2 && q < s.sq && (q < s.bq0 || q >= s.bq1)) {
-            // Empty slots get raw bits 0xFFFFFFFF, whose order key is 0.
-            const uint32_t m = quad_mask(s, q);
+    // Staged quads outside the body: at most one head and one tail quad,
+    // raw bits with 0xFFFFFFFF (order key 0) in the empty slots.
+    const int pq_q = tid < 1 ? 0 : s.nq - 1;
+    const bool pq_mine = tid < 2 && pq_q < s.sq && (pq_q < s.bq0 || pq_q >= s.bq1);
+    uint32_t pq[4] = {kFull, kFull, kFull, kFull};
+    if (pq_mine) {
+        const uint32_t m = quad_mask(s, pq_q);
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-                keys[4 * q + i] = ((m >> i) & 1u) ? __float_as_uint(__ldg(s.gptr + 4 * q + i)) : kFull;
-        }
+        for (int i = 0; i < 4; ++i)
+            if ((m >> i) & 1u) pq[i] = __float_as_uint(__ldg(s.gptr + 4 * pq_q + i));
     }
     for (int b = tid; b < 2 * kBins; b += THREADS) hist0[b] = 0u;
     if (tid == 0) {
@@ -2047,29 +2313,270 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
         ctrl.win_local = 0u;
         ctrl.wmin = kFull;
         ctrl.wmax = 0u;
+        ctrl.smax = 0u;
+        ctrl.overflow = 0u;
+        ctrl.cl_fb = 0u;
+        ctrl.maxbin = 0u;
+        ctrl.loc_begin = kFull;
+        ctrl.loc_end = 0u;
     }
     __syncthreads();
-    mbar_wait_bounded(&ctrl.bar, 0);
 
-    // ---- 2. level 0: keys in place, top-digit histogram, +0.0 counts ---- //
-    if (staged) level0_pass<THREADS, true>(ctrl, s, keys, pt, hist0, n_sentinel);
-    else level0_pass<THREADS, false>(ctrl, s, keys, pt, hist0, 0u);
+    // ---- 2. the candidate bound from the sample: the top digit of its
+    //         m-th largest key (m = k when the sample is the whole row) --- //
+    {
+        uint32_t smx = 0;
+#pragma unroll
+        for (int u = 0; u < SPT; ++u) {
+            if ((uint32_t)tid + (uint32_t)(u * THREADS) < S) {
+                const uint32_t e = order_key(skey[u]);
+                atomicAdd(&hist0[e >> 21], 1u);
+                smx = max(smx, e);
+            }
+        }
+        smx = __reduce_max_sync(kFull, smx);
+        if (lane == 0) atomicMax(&ctrl.smax, smx);
+    }
     __syncthreads();
+    uint32_t m_s = k_eff;
+    if (L > kSample) {
+        const float q = (float)k_eff / (float)L;
+        const float mu = (float)S * q;
+        const float m = ceilf(mu + 4.0f * sqrtf(mu * (1.0f - q)) + 8.0f);
+        m_s = m < (float)S ? (uint32_t)m : S;
+    }
+    {
+        uint32_t d, gt, c;
+        if (find_bin<THREADS>(hist0, m_s, ctrl.scan, d, gt, c)) ctrl.sel[0] = d;
+    }
+    __syncthreads();
+    // Candidates are the keys >= lo.  A bound on or below the +0.0 digit
+    // makes the candidates the positive keys, with +0.0 counted apart.
+    const uint32_t d_lo = ctrl.sel[0];
+    const bool plat = d_lo <= kZeroDigit;
+    const uint32_t lo = plat ? kZeroKey + 1u : d_lo << 21;
+    // Fine bins start at the smallest sampled key >= lo (candidates below it
+    // share bin 0) and the sample's range spans 512 of them.
+    {
+        uint32_t smn = kFull;
+#pragma unroll
+        for (int u = 0; u < SPT; ++u) {
+            const uint32_t e = order_key(skey[u]);
+            if ((uint32_t)tid + (uint32_t)(u * THREADS) < S && e >= lo) smn = min(smn, e);
+        }
+        smn = __reduce_min_sync(kFull, smn);
+        if (lane == 0) atomicMin(&ctrl.loc_begin, smn);   // loc_begin is free until the gather
+    }
+    __syncthreads();
+    const uint32_t f_lo = ctrl.loc_begin != kFull ? ctrl.loc_begin : lo;
+    const uint32_t smax = ctrl.smax;
+    const int span_bits = 32 - __clz(smax > f_lo ? smax - f_lo : 0u);
+    const uint32_t sh = span_bits > 9 ? (uint32_t)(span_bits - 9) : 0u;
+    if (pq_mine) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) keys[4 * pq_q + i] = pq[i];
+    }
+    mbar_wait_bounded(&ctrl.bar, 0);
+    __syncthreads();
+
+    // ---- 3. one pass: candidates to the fine histogram and the list ------ //
+    uint32_t *fhist = hist1;   // kFineBins words
+    if (plat) sampled_pass<THREADS, true>(ctrl, s, keys, ptm, fhist, win, wcap, lo, f_lo, sh);
+    else sampled_pass<THREADS, false>(ctrl, s, keys, ptm, fhist, win, wcap, lo, f_lo, sh);
+    if (tid == 0) ctrl.loc_begin = kFull;
+    __syncthreads();
+    cluster_sync();   // F0: every CTA's fine histogram, list and counts are final
+
+    // ---- 4. the group's counts, every fine bin's first output place ------ //
+    if (warp == 0) {
+        const uint32_t rk = g0 + (uint32_t)lane;
+        uint32_t cnt = 0, over = 0, z = 0;
+        if (lane < (int)gsize) {
+            if (rk == crank) {
+                cnt = ctrl.win_local;
+                over = ctrl.overflow;
+                z = ctrl.zeros;
+            } else {
+                cnt = dsmem_ld(dsmem_addr(&ctrl.win_local, rk));
+                over = dsmem_ld(dsmem_addr(&ctrl.overflow, rk));
+                z = plat ? dsmem_ld(dsmem_addr(&ctrl.zeros, rk)) : 0u;
+            }
+        }
+        if (lane < 16) ctrl.gcnt[lane] = cnt;
+        const uint32_t n_all = __reduce_add_sync(kFull, cnt);
+        const uint32_t z_all = __reduce_add_sync(kFull, z);
+        const uint32_t z_before = __reduce_add_sync(kFull, lane < (int)grank ? z : 0u);
+        const uint32_t over_any = __reduce_or_sync(kFull, over);
+        if (lane == 0) {
+            ctrl.tot[0] = n_all;
+            ctrl.tot[1] = z_all;
+            ctrl.tot[2] = over_any;
+            ctrl.gz_before = z_before;
+        }
+    }
+    constexpr int FB = kFineBins / THREADS;
+    const int flo = kFineBins - (tid + 1) * FB;   // thread 0 owns the top bins
+    uint32_t *offs = hist0;                       // first output place of each fine bin
+    uint32_t *cur = hist0 + kFineBins;            // placement cursors
+    {
+        uint32_t h[FB];
+#pragma unroll
+        for (int i = 0; i < FB; ++i) h[i] = fhist[flo + i];
+        for (uint32_t r0 = g0; r0 < g0 + gsize; ++r0) {
+            if (r0 == crank) continue;
+#pragma unroll
+            for (int i = 0; i < FB; ++i) h[i] += dsmem_ld(dsmem_addr(&fhist[flo + i], r0));
+        }
+        uint32_t hs = 0, hmax = 0;
+#pragma unroll
+        for (int i = 0; i < FB; ++i) {
+            hs += h[i];
+            hmax = max(hmax, h[i]);
+        }
+        hmax = __reduce_max_sync(kFull, hmax);
+        if (lane == 0) atomicMax(&ctrl.maxbin, hmax);
+        uint32_t run = block_incl_scan<THREADS>(hs, ctrl.scan) - hs;
+#pragma unroll
+        for (int i = FB - 1; i >= 0; --i) {
+            offs[flo + i] = run;
+            cur[flo + i] = run;
+            run += h[i];
+        }
+    }
+    const uint32_t n_bins_total = ctrl.scan[THREADS / 32 - 1];
+    __syncthreads();
+    const uint32_t n_all = ctrl.tot[0], z_all = ctrl.tot[1];
+    if (n_all != n_bins_total && tid == 0) atomicOr(&g_status, TOPK_DEV_INTERNAL);
+    const uint32_t loc_cap = (uint32_t)p.stage_cap / 2u;   // composites the staging area holds
+    bool fast = ctrl.tot[2] == 0u && n_all == n_bins_total && n_all <= loc_cap && ctrl.maxbin <= kMaxFineBin;
+    uint32_t n_out = k_eff, r_ties = 0;
+    if (fast) {
+        if (n_all >= k_eff) {
+            n_out = k_eff;                        // the k-th key is a candidate
+        } else if (plat && n_all + z_all >= k_eff) {
+            n_out = n_all;                        // the k-th key is +0.0
+            r_ties = k_eff - n_all;
+        } else {
+            fast = false;
+        }
+    }
+
+    // ---- 5. sampled path: this CTA's share of the output places --------- //
+    if (fast) {
+        if (r_ties > 0)
+            write_zero_ties<THREADS>(ctrl, s, keys, ptm, ctrl.gz_before, r_ties, n_out, k_eff, idx_offset, oi, ov,
+                                     excl);
+        __syncthreads();   // the staging area becomes the gather buffer
+        uint64_t *loc = reinterpret_cast<uint64_t *>(keys);
+        const uint32_t pos_lo = (uint32_t)((uint64_t)n_out * grank / gsize);
+        const uint32_t pos_hi = (uint32_t)((uint64_t)n_out * (grank + 1) / gsize);
+        // The group's lists as one index space (list gr at gpre[gr]); four
+        // remote loads per thread in flight at a time.
+        uint32_t n_lists = 0;
+        for (uint32_t gr = 0; gr < gsize; ++gr) n_lists += min(ctrl.gcnt[gr], wcap);
+        uint32_t lb = kFull, le = 0;
+        constexpr int G = 4;
+        for (uint32_t i0 = (uint32_t)tid; i0 < n_lists; i0 += G * THREADS) {
+            uint64_t c[G];
+#pragma unroll
+            for (int gg = 0; gg < G; ++gg) {
+                uint32_t i = i0 + (uint32_t)(gg * THREADS);
+                c[gg] = 0ull;
+                if (i >= n_lists) continue;
+                uint32_t gr = 0;
+                for (;;) {
+                    const uint32_t cnt = min(ctrl.gcnt[gr], wcap);
+                    if (i < cnt) break;
+                    i -= cnt;
+                    ++gr;
+                }
+                const uint32_t rk = g0 + gr;
+                c[gg] = rk == crank ? win[i] : dsmem_ld64(dsmem_addr(win, rk) + 8u * i);
+            }
+#pragma unroll
+            for (int gg = 0; gg < G; ++gg) {
+                if (i0 + (uint32_t)(gg * THREADS) >= n_lists) continue;
+                const uint32_t f = fine_bin((uint32_t)(c[gg] >> 32), f_lo, sh);
+                const uint32_t o = offs[f];
+                if (o >= pos_lo && o < pos_hi) {
+                    const uint32_t li = atomicAdd(&cur[f], 1u) - pos_lo;
+                    loc[li] = c[gg];
+                    lb = min(lb, li);
+                    le = max(le, li + 1u);
+                }
+            }
+        }
+        lb = __reduce_min_sync(kFull, lb);
+        le = __reduce_max_sync(kFull, le);
+        if (lane == 0 && le > 0) {
+            atomicMin(&ctrl.loc_begin, lb);
+            atomicMax(&ctrl.loc_end, le);
+        }
+        __syncthreads();
+        // A bin's members sit together at [offs - pos_lo, cur - pos_lo); a
+        // member's place is the bin's first place plus the members above it.
+        const uint32_t loc_end = ctrl.loc_end;
+        for (uint32_t i = ctrl.loc_begin + (uint32_t)tid; i < loc_end; i += THREADS) {
+            const uint64_t x = loc[i];
+            const uint32_t e = (uint32_t)(x >> 32);
+            const uint32_t f = fine_bin(e, f_lo, sh);
+            const uint32_t st = offs[f] - pos_lo, en = cur[f] - pos_lo;
+            uint32_t rank = 0;
+            for (uint32_t y = st; y < en; ++y) rank += loc[y] > x;
+            const uint32_t pos = offs[f] + rank;
+            if (pos < n_out) put_out(oi, ov, pos, idx_offset, (int32_t)(~(uint32_t)x), e, excl);
+        }
+        if (leader) pad_out(oi, ov, (int)k_eff, p.k);
+    } else if (tid < (int)csize) {
+        dsmem_st(dsmem_addr(&ctrl.cl_fb, (uint32_t)tid), 1u);   // the cluster runs the full select below
+    }
+    cluster_sync();   // F1: the group's lists are read; every fallback flag is set
+    const bool cluster_fallback = ctrl.cl_fb != 0u;
+    if (fast && leader && p.page_table) page_map_row(p, row, oi, (int)k_eff);
+    if (!cluster_fallback) return;
+
+    // ---- 6. the full radix select, for the groups whose checks failed;
+    //         every CTA of the cluster runs the same cluster barriers ------ //
+    const bool work = !fast;
+    if (work) {
+        for (int b = tid; b < 2 * kBins; b += THREADS) hist0[b] = 0u;
+        if (tid == 0) {
+            ctrl.zeros = 0u;
+            ctrl.win_local = 0u;
+            ctrl.wmin = kFull;
+            ctrl.wmax = 0u;
+        }
+        __syncthreads();
+        // level 0: keys in place, top-digit histogram, +0.0 counts
+        if (staged) level0_pass<THREADS, true>(ctrl, s, keys, pt, hist0, n_sentinel);
+        else level0_pass<THREADS, false>(ctrl, s, keys, pt, hist0, 0u);
+        __syncthreads();
+    }
     cluster_sync();   // B0: every CTA's level-0 histogram and counts are final
 
-    if (warp == 0) {
-        // The group's +0.0 count: lane l reads the group's l-th CTA.
-        const uint32_t rk = g0 + (uint32_t)lane;
-        uint32_t z = 0;
-        if (lane < (int)gsize) z = rk == crank ? ctrl.zeros : dsmem_ld(dsmem_addr(&ctrl.zeros, rk));
-        z = __reduce_add_sync(kFull, z);
-        if (lane == 0) ctrl.tot[0] = z;
-    }
     enum { kRefine = 0, kRange = 1, kExact = 2 };
     int mode = kRefine;
     uint32_t r = k_eff, n_gt = 0, prefix = 0, lo_key = 0, T = 0, n_cand = 0;
     bool plateau = false;
-    {
+    // Ties before this CTA in the group (plateau: +0.0 entries).
+    auto ties_before = [&](const uint32_t *src) {
+        if (warp == 0) {
+            uint32_t part = lane < (int)grank ? dsmem_ld(dsmem_addr(src, g0 + (uint32_t)lane)) : 0u;
+            part = __reduce_add_sync(kFull, part);
+            if (lane == 0) ctrl.scan[0] = part;
+        }
+        __syncthreads();
+        return ctrl.scan[0];
+    };
+    if (work) {
+        if (warp == 0) {
+            // The group's +0.0 count: lane l reads the group's l-th CTA.
+            const uint32_t rk = g0 + (uint32_t)lane;
+            uint32_t z = 0;
+            if (lane < (int)gsize) z = rk == crank ? ctrl.zeros : dsmem_ld(dsmem_addr(&ctrl.zeros, rk));
+            z = __reduce_add_sync(kFull, z);
+            if (lane == 0) ctrl.tot[0] = z;
+        }
         uint32_t d, gt, c;
         group_select<THREADS>(ctrl, hist0, g0, gsize, crank, r, d, gt, c);
         if (d == kZeroDigit && c == ctrl.tot[0]) {
@@ -2088,31 +2595,21 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
             n_gt = gt;
             r -= gt;
         }
-    }
-    // Ties before this CTA in the group (plateau: +0.0 entries).
-    auto ties_before = [&](const uint32_t *src) {
-        if (warp == 0) {
-            uint32_t part = lane < (int)grank ? dsmem_ld(dsmem_addr(src, g0 + (uint32_t)lane)) : 0u;
-            part = __reduce_add_sync(kFull, part);
-            if (lane == 0) ctrl.scan[0] = part;
+        if (mode != kRefine) {
+            if (plateau)
+                compact<THREADS, true>(staged, ctrl, s, keys, pt, ptm, win, wcap, 0u, T, ties_before(&ctrl.zeros), r,
+                                       n_gt, k_eff, idx_offset, oi, ov, excl);
+            else
+                compact<THREADS, false>(staged, ctrl, s, keys, pt, ptm, win, wcap, lo_key, 0u, 0u, r, n_gt, k_eff,
+                                        idx_offset, oi, ov, excl);
+        } else {
+            refine_pass<THREADS>(staged, s, keys, pt, ptm, hist1, prefix, 21, 10, 0x7FFu);
+            __syncthreads();
         }
-        __syncthreads();
-        return ctrl.scan[0];
-    };
-    if (mode != kRefine) {
-        if (plateau)
-            compact<THREADS, true>(staged, ctrl, s, keys, pt, ptm, win, wcap, 0u, T, ties_before(&ctrl.zeros), r,
-                                   n_gt, k_eff, idx_offset, oi, ov, excl);
-        else
-            compact<THREADS, false>(staged, ctrl, s, keys, pt, ptm, win, wcap, lo_key, 0u, 0u, r, n_gt, k_eff,
-                                    idx_offset, oi, ov, excl);
-    } else {
-        refine_pass<THREADS>(staged, s, keys, pt, ptm, hist1, prefix, 21, 10, 0x7FFu);
-        __syncthreads();
     }
     cluster_sync();   // B1
 
-    if (mode == kRefine) {
+    if (work && mode == kRefine) {
         uint32_t d, gt, c;
         group_select<THREADS>(ctrl, hist1, g0, gsize, crank, r, d, gt, c);
         if (n_gt + gt + c <= wcap) {
@@ -2121,7 +2618,7 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
             n_cand = n_gt + gt + c;
             compact<THREADS, false>(staged, ctrl, s, keys, pt, ptm, win, wcap, lo_key, 0u, 0u, r, n_gt, k_eff,
                                     idx_offset, oi, ov, excl);
-            } else {
+        } else {
             prefix = (prefix << 11) | d;
             n_gt += gt;
             r -= gt;
@@ -2134,7 +2631,7 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
     }
     cluster_sync();   // B2
 
-    if (mode == kRefine) {
+    if (work && mode == kRefine) {
         uint32_t d, gt, c;
         group_select<THREADS>(ctrl, hist0, g0, gsize, crank, r, d, gt, c);
         mode = kExact;
@@ -2147,12 +2644,12 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
     }
     cluster_sync();   // B3: every CTA's candidate list is final
 
-    // ---- 5. the leader gathers the group's lists into its staging area
+    // ---- 7. the leader gathers the group's lists into its staging area
     //         (its own keys are no longer needed), releases the peers and
     //         sorts; the peers wait until it has read their lists ---------- //
     uint64_t *cand = reinterpret_cast<uint64_t *>(keys);
     uint32_t n = 0;
-    if (leader) {
+    if (work && leader) {
         if (warp == 0) {
             const uint32_t rk = g0 + (uint32_t)lane;
             uint32_t cnt = 0, mn = kFull, mx = 0;
@@ -2188,15 +2685,15 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
         __syncthreads();
     }
     cluster_arrive();   // B4: the leaders have read every list
-    if (leader) {
+    if (work && leader) {
         const uint32_t expect = mode == kRange ? n_cand : n_gt;
         if (n != expect || n > wcap) {
             if (tid == 0) atomicOr(&g_status, TOPK_DEV_INTERNAL);
             n = min(min(n, expect), wcap);
         }
-        const uint32_t n_out = mode == kRange ? k_eff : n_gt;
+        const uint32_t n_o = mode == kRange ? k_eff : n_gt;
         if (n > 0) {
-            sort_and_write<THREADS>(cand, win, (int)n, (int)min(n, n_out), (int)wcap, ctrl.sel[1], ctrl.sel[2], hist0,
+            sort_and_write<THREADS>(cand, win, (int)n, (int)min(n, n_o), (int)wcap, ctrl.sel[1], ctrl.sel[2], hist0,
                                     ctrl.scan64, oi, ov, idx_offset, excl);
         }
         pad_out(oi, ov, (int)k_eff, p.k);
