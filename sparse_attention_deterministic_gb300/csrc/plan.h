@@ -48,7 +48,7 @@ struct alignas(16) Ctrl {
 
 // Per-CTA control block of the cluster kernel.
 struct alignas(16) CCtrl {
-    uint64_t bar;          // completion of the slice's bulk copies
+    uint64_t bar[8];       // completion of each 32 KB bulk copy of the staged slice
     uint32_t zeros;        // this CTA's count of exact +0.0 keys
     uint32_t win_local;    // entries in this CTA's candidate list
     uint32_t wmin;         // smallest candidate key in this CTA's list
@@ -65,7 +65,12 @@ struct alignas(16) CCtrl {
     // range of this CTA's share of the group's candidates in its buffer.
     uint32_t smax, overflow, cl_fb, maxbin;
     uint32_t loc_begin, loc_end, gz_before, pad0;
-    uint32_t gcnt[16];     // candidate-list lengths of the group's CTAs
+    // Counters of the group's CTAs (entry g from the group's CTA g, written
+    // into every CTA of the group before the cluster barrier).
+    uint32_t gcnt[16];     // candidate-list lengths
+    uint32_t gover[16];    // list overflow flags
+    uint32_t gzero[16];    // +0.0 counts
+    uint32_t gpos[17];     // first output place of each CTA's share (sampled path)
 };
 
 // Kernel variants: the one-CTA-per-row kernel and the cluster kernel at 512
@@ -107,11 +112,13 @@ inline int header_bytes(bool cluster)
 }
 
 // Candidate slots: the one-CTA kernel keeps the winners (fewer than k); the
-// cluster kernel's leader keeps up to twice k candidates, so that most rows
-// can be sorted after one or two histogram levels.
+// cluster kernel keeps up to twice k candidates per CTA.
 inline int list_cap(bool cluster, int k)
 {
-    return cluster ? 2 * next_pow2(k) : next_pow2(k - 1 > 1 ? k - 1 : 1);
+    // The cluster kernel's list also holds the two 2048-bin histograms of
+    // the row's sample before the candidates are appended: 2048 slots at
+    // least.
+    return cluster ? (2 * next_pow2(k) > 2048 ? 2 * next_pow2(k) : 2048) : next_pow2(k - 1 > 1 ? k - 1 : 1);
 }
 
 // Dynamic shared memory a CTA of the variant may use: all an SM has for the

@@ -2027,93 +2027,139 @@ __device__ __forceinline__ uint4 raw_body_quad(const Slice &s, const uint4 *raw4
     return make_uint4(__float_as_uint(f.x), __float_as_uint(f.y), __float_as_uint(f.z), __float_as_uint(f.w));
 }
 
-__device__ __forceinline__ int32_t quad_smax(const uint4 &r)
+// Appends a lane's candidates of one round (mask cm over U quads r[],
+// quad u at quad index q0 + 32 u) to the list as (raw bits << 32 | ~j):
+// slots from one warp scan and one shared-memory atomic per round.
+template <int U>
+__device__ __forceinline__ void append_round(CCtrl &ctrl, const Slice &s, const uint4 (&r)[U], uint32_t cm, int q0,
+                                             uint64_t *win, uint32_t wcap, bool &over)
 {
-    return max(max((int32_t)r.x, (int32_t)r.y), max((int32_t)r.z, (int32_t)r.w));
+    const int lane = threadIdx.x & 31;
+    const uint32_t cnt = (uint32_t)__popc(cm);
+    const uint32_t ci = warp_incl_scan(cnt);
+    uint32_t base = 0;
+    if (lane == 31) base = atomicAdd(&ctrl.win_local, ci);
+    uint32_t slot = __shfl_sync(kFull, base, 31) + ci - cnt;
+    while (cm) {
+        const int b = __ffs(cm) - 1;
+        cm &= cm - 1u;
+        const int u = b >> 2, i = b & 3;
+        uint4 x = r[0];
+#pragma unroll
+        for (int v = 1; v < U; ++v)
+            if (u == v) x = r[v];
+        const uint32_t val = i == 0 ? x.x : i == 1 ? x.y : i == 2 ? x.z : x.w;
+        const uint32_t j = (uint32_t)(s.jbase + 4 * (q0 + 32 * u) + i);
+        if (slot < wcap) win[slot] = ((uint64_t)val << 32) | (uint64_t)(~j);
+        else over = true;
+        ++slot;
+    }
 }
 
-// The pass over the slice: keys >= lo go to the fine histogram and to the
-// candidate list (slots from one shared-memory atomic per warp round; a
-// slot past wcap sets ctrl.overflow); with PLATEAU the +0.0 entries are
-// counted per warp in index order (ctrl.warp_zeros) and in all (ctrl.zeros).
-// lo is above the +0.0 key, so key >= lo holds exactly when the raw bits,
-// read as a signed integer, are >= lo_raw = lo - 0x80000000 (every negative
-// pattern is below every non-negative one): the scan compares raw bits and
-// only candidates are turned into keys.
-template <int THREADS, bool PLATEAU>
-__device__ void sampled_pass(CCtrl &ctrl, const Slice &s, const uint32_t *raw, const Parts &pt, uint32_t *fhist,
-                             uint64_t *win, uint32_t wcap, uint32_t lo, uint32_t f_lo, uint32_t sh)
+// Candidate mask of a lane's round: bit 4u + i for element i of quad u.
+template <int U>
+__device__ __forceinline__ uint32_t cand_mask(const uint4 (&r)[U], int32_t lo_raw)
 {
-    constexpr int U = kPassQuads;
+    uint32_t cm = 0;
+#pragma unroll
+    for (int u = 0; u < U; ++u)
+        cm |= ((uint32_t)((int32_t)r[u].x >= lo_raw) | (uint32_t)((int32_t)r[u].y >= lo_raw) << 1 |
+               (uint32_t)((int32_t)r[u].z >= lo_raw) << 2 | (uint32_t)((int32_t)r[u].w >= lo_raw) << 3)
+              << (4 * u);
+    return cm;
+}
+
+__device__ __forceinline__ uint32_t zero_count(const uint4 &r)
+{
+    return (uint32_t)(r.x == 0u) + (uint32_t)(r.y == 0u) + (uint32_t)(r.z == 0u) + (uint32_t)(r.w == 0u);
+}
+
+// The pass over the slice: keys >= lo go to the candidate list, as raw bits
+// and index (finish_candidates turns them into composites and counts them
+// into the fine histogram); a slot past wcap sets ctrl.overflow.  With
+// PLATEAU the +0.0 entries are counted per warp in index order
+// (ctrl.warp_zeros) and in all (ctrl.zeros).  lo is above the +0.0 key, so
+// key >= lo holds exactly when the raw bits, read as a signed integer, are
+// >= lo_raw = lo - 0x80000000 (every negative pattern is below every
+// non-negative one): the scan compares raw bits, four quads per lane per
+// round, and a round with no candidate in the warp costs a few instructions
+// per quad.
+template <int THREADS, bool PLATEAU>
+__device__ void sampled_pass(CCtrl &ctrl, const Slice &s, const uint32_t *raw, const Parts &pt, uint64_t *win,
+                             uint32_t wcap, uint32_t lo, int q_copy_end)
+{
+    constexpr int U = 4;
+    constexpr int kChunkQuads = 2048;   // quads per 32 KB copy
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const uint4 *raw4 = reinterpret_cast<const uint4 *>(raw);
     const int32_t lo_raw = (int32_t)(lo - 0x80000000u);
+    // The copies under this warp's run of bulk-copied quads.
+    {
+        const int c_end = pt.q1 < q_copy_end ? pt.q1 : q_copy_end;
+        if (c_end > pt.q0)
+            for (int c = (pt.q0 - s.bq0) / kChunkQuads; c <= (c_end - 1 - s.bq0) / kChunkQuads; ++c)
+                mbar_wait_bounded(&ctrl.bar[c], 0);
+    }
     uint32_t zeros = 0;
     bool over = false;
-    auto put = [&](uint32_t u, int32_t j, uint32_t slot) {
-        const uint32_t e = order_key(u);
-        atomicAdd(&fhist[fine_bin(e, f_lo, sh)], 1u);
-        if (slot < wcap) win[slot] = ((uint64_t)e << 32) | (uint64_t)(~(uint32_t)j);
-        else over = true;
-    };
     auto partial = [&](int q) {
-        uint32_t m;
-        uint4 r;
-        if (q < s.sq) {
-            m = quad_mask(s, q);
-            r = raw4[q];
-        } else {
-            m = quad_mask(s, q);
-            uint32_t e[4];
+        const uint32_t m = quad_mask(s, q);
+        uint32_t u4[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i) e[i] = ((m >> i) & 1u) ? __float_as_uint(__ldg(s.gptr + 4 * q + i)) : 0u;
-            r = make_uint4(e[0], e[1], e[2], e[3]);
-        }
-        const uint32_t u4[4] = {r.x, r.y, r.z, r.w};
+        for (int i = 0; i < 4; ++i)
+            u4[i] = !((m >> i) & 1u) ? 0xFFFFFFFFu : q < s.sq ? raw[4 * q + i] : __float_as_uint(__ldg(s.gptr + 4 * q + i));
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             if (!((m >> i) & 1u)) continue;
             if (PLATEAU) zeros += u4[i] == 0u;
-            if ((int32_t)u4[i] >= lo_raw) put(u4[i], s.jbase + 4 * q + i, atomicAdd(&ctrl.win_local, 1u));
+            if ((int32_t)u4[i] >= lo_raw) {
+                const uint32_t slot = atomicAdd(&ctrl.win_local, 1u);
+                const uint32_t j = (uint32_t)(s.jbase + 4 * q + i);
+                if (slot < wcap) win[slot] = ((uint64_t)u4[i] << 32) | (uint64_t)(~j);
+                else over = true;
+            }
         }
     };
     if (lane == 0 && pt.head >= 0) partial(pt.head);
-    for (int qb = pt.q0; qb < pt.q1; qb += 32 * U) {
-        uint4 rr[U];
+    // Staged quads: full rounds of U quads per lane from shared memory.
+    const int q_st = pt.q1 < s.sq ? pt.q1 : (pt.q0 > s.sq ? pt.q0 : s.sq);   // end of the staged run
+    const uint4 *raw4 = reinterpret_cast<const uint4 *>(raw) + lane;
+    int qb = pt.q0;
+    for (; qb + 32 * U <= q_st; qb += 32 * U) {
+        uint4 r[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) {
-            const int q = qb + u * 32 + lane;
-            // Quads past the run read as -1 (below every bound, never +0.0).
-            rr[u] = q < pt.q1 ? raw_body_quad(s, raw4, q) : make_uint4(kFull, kFull, kFull, kFull);
+        for (int u = 0; u < U; ++u) r[u] = raw4[qb + 32 * u];
+        int32_t mq[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            mq[u] = max(max((int32_t)r[u].x, (int32_t)r[u].y), max((int32_t)r[u].z, (int32_t)r[u].w));
+        const int32_t m = max(max(mq[0], mq[1]), max(mq[2], mq[3]));
+        if (PLATEAU) {
+#pragma unroll
+            for (int u = 0; u < U; ++u) zeros += zero_count(r[u]);
         }
-        uint32_t cm = 0;
+        if (__any_sync(kFull, m >= lo_raw)) append_round<U>(ctrl, s, r, cand_mask<U>(r, lo_raw), qb + lane, win, wcap, over);
+    }
+    // The rest of the run (a partial round, and quads beyond the staging
+    // area, read where they lie), with per-quad checks.
+    for (; qb < pt.q1; qb += 32 * U) {
+        uint4 r[U];
+        uint32_t okm = 0;
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            if (PLATEAU)
-                zeros += (uint32_t)(rr[u].x == 0u) + (uint32_t)(rr[u].y == 0u) + (uint32_t)(rr[u].z == 0u) +
-                         (uint32_t)(rr[u].w == 0u);
-            if (quad_smax(rr[u]) >= lo_raw) {
-                cm |= ((uint32_t)((int32_t)rr[u].x >= lo_raw) | (uint32_t)((int32_t)rr[u].y >= lo_raw) << 1 |
-                       (uint32_t)((int32_t)rr[u].z >= lo_raw) << 2 | (uint32_t)((int32_t)rr[u].w >= lo_raw) << 3)
-                      << (4 * u);
+            const int q = qb + 32 * u + lane;
+            r[u] = make_uint4(kFull, kFull, kFull, kFull);
+            if (q < pt.q1) {
+                okm |= 1u << u;
+                r[u] = raw_body_quad(s, reinterpret_cast<const uint4 *>(raw), q);
             }
         }
-        if (!__any_sync(kFull, cm != 0)) continue;
-        const uint32_t cnt = (uint32_t)__popc(cm);
-        const uint32_t ci = warp_incl_scan(cnt);
-        uint32_t base = 0;
-        if (lane == 31) base = atomicAdd(&ctrl.win_local, ci);
-        uint32_t slot = __shfl_sync(kFull, base, 31) + ci - cnt;
-        // One step per candidate of this lane (a few per round), not one
-        // per slot of the round.
-        while (cm) {
-            const int b = __ffs(cm) - 1;
-            cm &= cm - 1u;
-            const int u = b >> 2, i = b & 3;
-            const uint4 r = u == 0 ? rr[0] : rr[U - 1];
-            const uint32_t v = i == 0 ? r.x : i == 1 ? r.y : i == 2 ? r.z : r.w;
-            put(v, s.jbase + 4 * (qb + u * 32 + lane) + i, slot++);
+        if (PLATEAU) {
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if ((okm >> u) & 1u) zeros += zero_count(r[u]);
         }
+        const uint32_t cm = cand_mask<U>(r, lo_raw);   // -1 fill is below every bound
+        if (__any_sync(kFull, cm != 0)) append_round<U>(ctrl, s, r, cm, qb + lane, win, wcap, over);
     }
     if (lane == 0 && pt.tail >= 0) partial(pt.tail);
     if (over) atomicOr(&ctrl.overflow, 1u);
@@ -2123,6 +2169,121 @@ __device__ void sampled_pass(CCtrl &ctrl, const Slice &s, const uint32_t *raw, c
             ctrl.warp_zeros[warp] = zeros;
             if (zeros) atomicAdd(&ctrl.zeros, zeros);
         }
+    }
+}
+
+// The pass in two phases, for slices of at most kMaskRounds rounds of four
+// quads per lane: first each lane keeps, per round (16 entries), a 16-bit
+// mask of its candidates in a register (no votes, scans or atomics in the
+// scan); then one block scan of the per-thread candidate counts gives every
+// thread its slots, and each thread writes its own candidates as composites
+// (order key << 32 | ~j), counting each into the fine histogram.  The
+// partial head and tail quads are appended first (slots by atomics).
+// Counts +0.0 like sampled_pass; leaves the list length in ctrl.win_local.
+constexpr int kMaskRounds = 4;
+
+template <int THREADS>
+__device__ __forceinline__ int mask_rounds(const Slice &s)
+{
+    constexpr int NW = THREADS / 32;
+    const int n = s.bq1 - s.bq0, per = (n + NW - 1) / NW;
+    return (per + 127) / 128;
+}
+
+template <int THREADS, bool PLATEAU, bool STAGED>
+__device__ void masked_pass(CCtrl &ctrl, const Slice &s, const uint32_t *raw, const Parts &pt, uint64_t *win,
+                            uint32_t wcap, int R, uint32_t lo, uint32_t *fhist, uint32_t f_lo, uint32_t sh,
+                            int q_copy_end)
+{
+    constexpr int U = 4;
+    constexpr int kChunkQuads = 2048;   // quads per 32 KB copy
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int32_t lo_raw = (int32_t)(lo - 0x80000000u);
+    const uint4 *raw4 = reinterpret_cast<const uint4 *>(raw);
+    {
+        const int c_end = pt.q1 < q_copy_end ? pt.q1 : q_copy_end;
+        if (c_end > pt.q0)
+            for (int c = (pt.q0 - s.bq0) / kChunkQuads; c <= (c_end - 1 - s.bq0) / kChunkQuads; ++c)
+                mbar_wait_bounded(&ctrl.bar[c], 0);
+    }
+    uint32_t zeros = 0;
+    bool over = false;
+    auto put = [&](uint32_t u, uint32_t j, uint32_t slot) {
+        const uint32_t e = order_key(u);
+        atomicAdd(&fhist[fine_bin(e, f_lo, sh)], 1u);
+        if (slot < wcap) win[slot] = ((uint64_t)e << 32) | (uint64_t)(~j);
+        else over = true;
+    };
+    auto partial = [&](int q) {
+        const uint32_t m = quad_mask(s, q);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            if (!((m >> i) & 1u)) continue;
+            const uint32_t u = q < s.sq ? raw[4 * q + i] : __float_as_uint(__ldg(s.gptr + 4 * q + i));
+            if (PLATEAU) zeros += u == 0u;
+            if ((int32_t)u >= lo_raw) put(u, (uint32_t)(s.jbase + 4 * q + i), atomicAdd(&ctrl.win_local, 1u));
+        }
+    };
+    if (lane == 0 && pt.head >= 0) partial(pt.head);
+    if (lane == 0 && pt.tail >= 0) partial(pt.tail);
+    // Phase 1: round r covers quads pt.q0 + 128 r + 32 u + lane.
+    uint32_t mk[kMaskRounds];
+    uint32_t cnt = 0;
+#pragma unroll
+    for (int r = 0; r < kMaskRounds; ++r) {
+        mk[r] = 0u;
+        if (r >= R) continue;
+        const int qb = pt.q0 + 128 * r + lane;
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int q = qb + 32 * u;
+            if (q < pt.q1) {
+                const uint4 x = STAGED ? raw4[q] : raw_body_quad(s, raw4, q);
+                if (PLATEAU) zeros += zero_count(x);
+                mk[r] |= ((uint32_t)((int32_t)x.x >= lo_raw) | (uint32_t)((int32_t)x.y >= lo_raw) << 1 |
+                          (uint32_t)((int32_t)x.z >= lo_raw) << 2 | (uint32_t)((int32_t)x.w >= lo_raw) << 3)
+                         << (4 * u);
+            }
+        }
+        cnt += (uint32_t)__popc(mk[r]);
+    }
+    if (PLATEAU) {
+        zeros = __reduce_add_sync(kFull, zeros);
+        if (lane == 0) {
+            ctrl.warp_zeros[warp] = zeros;
+            if (zeros) atomicAdd(&ctrl.zeros, zeros);
+        }
+    }
+    __syncthreads();   // the head and tail entries are counted
+    // Phase 2: slots after the head and tail entries, in thread order.
+    const uint32_t base = ctrl.win_local;
+    uint32_t slot = base + block_incl_scan<THREADS>(cnt, ctrl.scan) - cnt;
+    if (tid == THREADS - 1) ctrl.win_local = slot + cnt;   // read by the caller after a barrier
+#pragma unroll
+    for (int r = 0; r < kMaskRounds; ++r) {
+        uint32_t m = mk[r];
+        const int qb = pt.q0 + 128 * r + lane;
+        while (m) {
+            const int b = __ffs(m) - 1;
+            m &= m - 1u;
+            const int q = qb + 32 * (b >> 2), i = b & 3;
+            const uint32_t u = STAGED || q < s.sq ? raw[4 * q + i] : __float_as_uint(__ldg(s.gptr + 4 * q + i));
+            put(u, (uint32_t)(s.jbase + 4 * q + i), slot++);
+        }
+    }
+    if (over) atomicOr(&ctrl.overflow, 1u);
+}
+
+// The CTA's candidates, appended as (raw bits << 32 | ~j), become composites
+// (order key << 32 | ~j) and are counted into the fine histogram.
+template <int THREADS>
+__device__ __forceinline__ void finish_candidates(uint64_t *win, uint32_t n, uint32_t *fhist, uint32_t f_lo, uint32_t sh)
+{
+    for (uint32_t i = threadIdx.x; i < n; i += THREADS) {
+        const uint64_t x = win[i];
+        const uint32_t e = order_key((uint32_t)(x >> 32));
+        win[i] = ((uint64_t)e << 32) | (x & 0xFFFFFFFFull);
+        atomicAdd(&fhist[fine_bin(e, f_lo, sh)], 1u);
     }
 }
 
@@ -2199,36 +2360,42 @@ __device__ void write_zero_ties(CCtrl &ctrl, const Slice &s, const uint32_t *raw
     if (pt.tail >= 0 && tbase < r) partial(pt.tail);
 }
 
-// Remote store into the shared memory of cluster CTA `rank`.
+// Remote stores into the shared memory of a cluster CTA (addresses from
+// dsmem_addr).
 __device__ __forceinline__ void dsmem_st(uint32_t addr, uint32_t v)
 {
     asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
-template <int THREADS>
-__global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kernel(const Params p)
+__device__ __forceinline__ void dsmem_st64(uint32_t addr, uint64_t v)
 {
-    grid_dependency_enter();
+    asm volatile("st.shared::cluster.u64 [%0], %1;" ::"r"(addr), "l"(v) : "memory");
+}
+
+// The full radix select of a row group, out of line (it is the rare path of
+// the cluster kernel and keeping it out of the common path keeps that path's
+// code small): level 0 over the staged slice, then the threshold search and
+// refinement levels, compaction, and the leader's gather, sort and write.
+// Every CTA of the cluster calls it when any group of the cluster needs it,
+// with work = false in the groups that are done, and runs the same cluster
+// barriers.
+template <int THREADS>
+__device__ __noinline__ void full_select(const Params &p, const Slice &s, const RowGroup g, const bool work)
+{
     constexpr uint32_t kZeroKey = 0x80000000u;   // order key of +0.0
     constexpr uint32_t kZeroDigit = kZeroKey >> 21;
-    constexpr uint32_t kChunk = 32768;           // bytes per bulk copy
     extern __shared__ __align__(16) unsigned char smem[];
     CCtrl &ctrl = *reinterpret_cast<CCtrl *>(smem);
     uint32_t *hist0 = reinterpret_cast<uint32_t *>(smem + sizeof(CCtrl));   // levels 0 and 2
     uint32_t *hist1 = hist0 + kBins;                                          // level 1
     uint64_t *win = reinterpret_cast<uint64_t *>(smem + p.off_win);
     uint32_t *keys = reinterpret_cast<uint32_t *>(smem + p.off_keys);
-    const uint32_t wcap = (uint32_t)p.win_cap;   // candidate list capacity (a power of two)
-
+    const uint32_t wcap = (uint32_t)p.win_cap;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const uint32_t crank = cluster_rank(), csize = cluster_size();
-    const RowGroup g = assign_rows<THREADS>(p, crank, csize, hist0, ctrl.scan);
-    if (g.row < 0) return;   // uniform over the cluster: nothing to select
+    const uint32_t crank = cluster_rank();
     const int row = g.row;
     const uint32_t g0 = g.g0, gsize = g.gsize, grank = crank - g0;
     const bool leader = grank == 0;
-
-    // Rows handed out by assign_rows have 0 < L < 2^24 and a valid window.
     const int64_t rs = g.start;
     const int32_t L = g.len;
     const uint32_t k_eff = (uint32_t)(p.k < L ? p.k : L);
@@ -2236,308 +2403,17 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
     const bool excl = (p.offset_mode & TOPK_EXCLUDE_NEG_INF) != 0;
     int32_t *oi = p.out_idx + (int64_t)row * p.k;
     float *ov = p.out_val ? p.out_val + (int64_t)row * p.k : nullptr;
-
-    Slice s;
-    {
-        const uint64_t pa = (uint64_t)(uintptr_t)p.scores >> 2;   // element address
-        const int64_t e0 = rs, e1 = rs + L;
-        int64_t a0 = e0 + (int64_t)((4u - (uint32_t)((pa + (uint64_t)e0) & 3u)) & 3u);
-        if (a0 > e1) a0 = e1;
-        const int64_t n4 = (e1 - a0) >> 2;
-        // n4 < 2^22 and gsize <= 16: the products fit 32 bits.
-        const int64_t qlo = (uint32_t)n4 * grank / gsize, qhi = (uint32_t)n4 * (grank + 1) / gsize;
-        const int64_t hb = a0 + 4 * qlo, he = a0 + 4 * qhi;
-        const int64_t glo = grank == 0 ? e0 : hb;
-        const int64_t ghi = grank == gsize - 1 ? e1 : he;
-        const int64_t sbase = hb - ((hb - glo + 3) & ~(int64_t)3);
-        s.gptr = p.scores + sbase;
-        s.off0 = (int32_t)(glo - sbase);
-        s.end = (int32_t)(ghi - sbase);
-        s.bq0 = (int32_t)((hb - sbase) >> 2);
-        s.bq1 = (int32_t)((he - sbase) >> 2);
-        s.nq = (s.end + 3) >> 2;
-        s.sq = s.nq < (p.stage_cap >> 2) ? s.nq : (p.stage_cap >> 2);
-        s.jbase = (int32_t)(sbase - rs);
-    }
-    // A slice held entirely in shared memory runs the passes mask-free
-    // (staged_parts); otherwise the full quads, the partial end quads and
-    // the part beyond the staging area are read as they lie.
-    const bool staged = s.sq == s.nq;   // CTA-uniform
+    const bool staged = s.sq == s.nq;
     const Parts pt = staged ? staged_parts<THREADS>(s, warp) : slice_parts<THREADS>(s, warp);
-    const Parts ptm = slice_parts<THREADS>(s, warp);   // masked parts (key-0 ranges)
+    const Parts ptm = slice_parts<THREADS>(s, warp);
     const uint32_t n_sentinel = (uint32_t)(4 * s.nq - (s.end - s.off0));
-
-    // ---- 1. the row's sample, then the bulk copies (TMA) of the staged
-    //         body; the sample and the partial head and tail quads are
-    //         read with plain loads into registers, the sample first so
-    //         that it is not queued behind the copies ------------------- //
-    // The sample: the whole row when L <= kSample, else 128 runs of 32
-    // consecutive scores spread evenly over the row (run t starts at
-    // t * (L - 32) / 127), so that it costs a few cache lines per row rather
-    // than a read of most of the row's DRAM bursts.  The same in every CTA
-    // of the group (raw bits; keys after the barrier).
-    constexpr int SPT = kSample / THREADS;
-    static_assert(kPassQuads == 2, "the append step below reads the round's two quads");
-    const uint32_t S = (uint32_t)(L < kSample ? L : kSample);
-    uint32_t skey[SPT];
-#pragma unroll
-    for (int u = 0; u < SPT; ++u) {
-        const uint32_t t = (uint32_t)tid + (uint32_t)(u * THREADS);
-        const uint32_t j = L <= kSample ? t : (t >> 5) * (uint32_t)(L - 32) / 127u + (t & 31u);
-        skey[u] = t < S ? __float_as_uint(__ldg(p.scores + rs + j)) : 0u;
-    }
-    const int bq_end = s.bq1 < s.sq ? s.bq1 : s.sq;
-    if (tid == 0) {
-        mbar_init(&ctrl.bar, 1);
-        const uint32_t bytes = bq_end > s.bq0 ? 16u * (uint32_t)(bq_end - s.bq0) : 0u;
-        mbar_arrive_expect_tx(&ctrl.bar, bytes);
-        for (uint32_t off = 0; off < bytes; off += kChunk)
-            bulk_load(reinterpret_cast<unsigned char *>(keys + 4 * s.bq0) + off,
-                      reinterpret_cast<const unsigned char *>(s.gptr + 4 * s.bq0) + off,
-                      bytes - off < kChunk ? bytes - off : kChunk, &ctrl.bar);
-    }
-    // Staged quads outside the body: at most one head and one tail quad,
-    // raw bits with 0xFFFFFFFF (order key 0) in the empty slots.
-    const int pq_q = tid < 1 ? 0 : s.nq - 1;
-    const bool pq_mine = tid < 2 && pq_q < s.sq && (pq_q < s.bq0 || pq_q >= s.bq1);
-    uint32_t pq[4] = {kFull, kFull, kFull, kFull};
-    if (pq_mine) {
-        const uint32_t m = quad_mask(s, pq_q);
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-            if ((m >> i) & 1u) pq[i] = __float_as_uint(__ldg(s.gptr + 4 * pq_q + i));
-    }
-    for (int b = tid; b < 2 * kBins; b += THREADS) hist0[b] = 0u;
-    if (tid == 0) {
-        ctrl.zeros = 0u;
-        ctrl.win_local = 0u;
-        ctrl.wmin = kFull;
-        ctrl.wmax = 0u;
-        ctrl.smax = 0u;
-        ctrl.overflow = 0u;
-        ctrl.cl_fb = 0u;
-        ctrl.maxbin = 0u;
-        ctrl.loc_begin = kFull;
-        ctrl.loc_end = 0u;
-    }
-    __syncthreads();
-
-    // ---- 2. the candidate bound from the sample: the top digit of its
-    //         m-th largest key (m = k when the sample is the whole row) --- //
     {
-        uint32_t smx = 0;
-#pragma unroll
-        for (int u = 0; u < SPT; ++u) {
-            if ((uint32_t)tid + (uint32_t)(u * THREADS) < S) {
-                const uint32_t e = order_key(skey[u]);
-                atomicAdd(&hist0[e >> 21], 1u);
-                smx = max(smx, e);
-            }
-        }
-        smx = __reduce_max_sync(kFull, smx);
-        if (lane == 0) atomicMax(&ctrl.smax, smx);
+        // Every copy has landed (the sampled pass waited on each); waiting
+        // again returns at once and orders this thread after the copies.
+        const int bq_end = s.bq1 < s.sq ? s.bq1 : s.sq;
+        const uint32_t n_chunks = bq_end > s.bq0 ? (16u * (uint32_t)(bq_end - s.bq0) + 32767u) / 32768u : 0u;
+        for (uint32_t c = 0; c < n_chunks; ++c) mbar_wait_bounded(&ctrl.bar[c], 0);
     }
-    __syncthreads();
-    uint32_t m_s = k_eff;
-    if (L > kSample) {
-        const float q = (float)k_eff / (float)L;
-        const float mu = (float)S * q;
-        const float m = ceilf(mu + 4.0f * sqrtf(mu * (1.0f - q)) + 8.0f);
-        m_s = m < (float)S ? (uint32_t)m : S;
-    }
-    {
-        uint32_t d, gt, c;
-        if (find_bin<THREADS>(hist0, m_s, ctrl.scan, d, gt, c)) ctrl.sel[0] = d;
-    }
-    __syncthreads();
-    // Candidates are the keys >= lo.  A bound on or below the +0.0 digit
-    // makes the candidates the positive keys, with +0.0 counted apart.
-    const uint32_t d_lo = ctrl.sel[0];
-    const bool plat = d_lo <= kZeroDigit;
-    const uint32_t lo = plat ? kZeroKey + 1u : d_lo << 21;
-    // Fine bins start at the smallest sampled key >= lo (candidates below it
-    // share bin 0) and the sample's range spans 512 of them.
-    {
-        uint32_t smn = kFull;
-#pragma unroll
-        for (int u = 0; u < SPT; ++u) {
-            const uint32_t e = order_key(skey[u]);
-            if ((uint32_t)tid + (uint32_t)(u * THREADS) < S && e >= lo) smn = min(smn, e);
-        }
-        smn = __reduce_min_sync(kFull, smn);
-        if (lane == 0) atomicMin(&ctrl.loc_begin, smn);   // loc_begin is free until the gather
-    }
-    __syncthreads();
-    const uint32_t f_lo = ctrl.loc_begin != kFull ? ctrl.loc_begin : lo;
-    const uint32_t smax = ctrl.smax;
-    const int span_bits = 32 - __clz(smax > f_lo ? smax - f_lo : 0u);
-    const uint32_t sh = span_bits > 9 ? (uint32_t)(span_bits - 9) : 0u;
-    if (pq_mine) {
-#pragma unroll
-        for (int i = 0; i < 4; ++i) keys[4 * pq_q + i] = pq[i];
-    }
-    mbar_wait_bounded(&ctrl.bar, 0);
-    __syncthreads();
-
-    // ---- 3. one pass: candidates to the fine histogram and the list ------ //
-    uint32_t *fhist = hist1;   // kFineBins words
-    if (plat) sampled_pass<THREADS, true>(ctrl, s, keys, ptm, fhist, win, wcap, lo, f_lo, sh);
-    else sampled_pass<THREADS, false>(ctrl, s, keys, ptm, fhist, win, wcap, lo, f_lo, sh);
-    if (tid == 0) ctrl.loc_begin = kFull;
-    __syncthreads();
-    cluster_sync();   // F0: every CTA's fine histogram, list and counts are final
-
-    // ---- 4. the group's counts, every fine bin's first output place ------ //
-    if (warp == 0) {
-        const uint32_t rk = g0 + (uint32_t)lane;
-        uint32_t cnt = 0, over = 0, z = 0;
-        if (lane < (int)gsize) {
-            if (rk == crank) {
-                cnt = ctrl.win_local;
-                over = ctrl.overflow;
-                z = ctrl.zeros;
-            } else {
-                cnt = dsmem_ld(dsmem_addr(&ctrl.win_local, rk));
-                over = dsmem_ld(dsmem_addr(&ctrl.overflow, rk));
-                z = plat ? dsmem_ld(dsmem_addr(&ctrl.zeros, rk)) : 0u;
-            }
-        }
-        if (lane < 16) ctrl.gcnt[lane] = cnt;
-        const uint32_t n_all = __reduce_add_sync(kFull, cnt);
-        const uint32_t z_all = __reduce_add_sync(kFull, z);
-        const uint32_t z_before = __reduce_add_sync(kFull, lane < (int)grank ? z : 0u);
-        const uint32_t over_any = __reduce_or_sync(kFull, over);
-        if (lane == 0) {
-            ctrl.tot[0] = n_all;
-            ctrl.tot[1] = z_all;
-            ctrl.tot[2] = over_any;
-            ctrl.gz_before = z_before;
-        }
-    }
-    constexpr int FB = kFineBins / THREADS;
-    const int flo = kFineBins - (tid + 1) * FB;   // thread 0 owns the top bins
-    uint32_t *offs = hist0;                       // first output place of each fine bin
-    uint32_t *cur = hist0 + kFineBins;            // placement cursors
-    {
-        uint32_t h[FB];
-#pragma unroll
-        for (int i = 0; i < FB; ++i) h[i] = fhist[flo + i];
-        for (uint32_t r0 = g0; r0 < g0 + gsize; ++r0) {
-            if (r0 == crank) continue;
-#pragma unroll
-            for (int i = 0; i < FB; ++i) h[i] += dsmem_ld(dsmem_addr(&fhist[flo + i], r0));
-        }
-        uint32_t hs = 0, hmax = 0;
-#pragma unroll
-        for (int i = 0; i < FB; ++i) {
-            hs += h[i];
-            hmax = max(hmax, h[i]);
-        }
-        hmax = __reduce_max_sync(kFull, hmax);
-        if (lane == 0) atomicMax(&ctrl.maxbin, hmax);
-        uint32_t run = block_incl_scan<THREADS>(hs, ctrl.scan) - hs;
-#pragma unroll
-        for (int i = FB - 1; i >= 0; --i) {
-            offs[flo + i] = run;
-            cur[flo + i] = run;
-            run += h[i];
-        }
-    }
-    const uint32_t n_bins_total = ctrl.scan[THREADS / 32 - 1];
-    __syncthreads();
-    const uint32_t n_all = ctrl.tot[0], z_all = ctrl.tot[1];
-    if (n_all != n_bins_total && tid == 0) atomicOr(&g_status, TOPK_DEV_INTERNAL);
-    const uint32_t loc_cap = (uint32_t)p.stage_cap / 2u;   // composites the staging area holds
-    bool fast = ctrl.tot[2] == 0u && n_all == n_bins_total && n_all <= loc_cap && ctrl.maxbin <= kMaxFineBin;
-    uint32_t n_out = k_eff, r_ties = 0;
-    if (fast) {
-        if (n_all >= k_eff) {
-            n_out = k_eff;                        // the k-th key is a candidate
-        } else if (plat && n_all + z_all >= k_eff) {
-            n_out = n_all;                        // the k-th key is +0.0
-            r_ties = k_eff - n_all;
-        } else {
-            fast = false;
-        }
-    }
-
-    // ---- 5. sampled path: this CTA's share of the output places --------- //
-    if (fast) {
-        if (r_ties > 0)
-            write_zero_ties<THREADS>(ctrl, s, keys, ptm, ctrl.gz_before, r_ties, n_out, k_eff, idx_offset, oi, ov,
-                                     excl);
-        __syncthreads();   // the staging area becomes the gather buffer
-        uint64_t *loc = reinterpret_cast<uint64_t *>(keys);
-        const uint32_t pos_lo = (uint32_t)((uint64_t)n_out * grank / gsize);
-        const uint32_t pos_hi = (uint32_t)((uint64_t)n_out * (grank + 1) / gsize);
-        // The group's lists as one index space (list gr at gpre[gr]); four
-        // remote loads per thread in flight at a time.
-        uint32_t n_lists = 0;
-        for (uint32_t gr = 0; gr < gsize; ++gr) n_lists += min(ctrl.gcnt[gr], wcap);
-        uint32_t lb = kFull, le = 0;
-        constexpr int G = 4;
-        for (uint32_t i0 = (uint32_t)tid; i0 < n_lists; i0 += G * THREADS) {
-            uint64_t c[G];
-#pragma unroll
-            for (int gg = 0; gg < G; ++gg) {
-                uint32_t i = i0 + (uint32_t)(gg * THREADS);
-                c[gg] = 0ull;
-                if (i >= n_lists) continue;
-                uint32_t gr = 0;
-                for (;;) {
-                    const uint32_t cnt = min(ctrl.gcnt[gr], wcap);
-                    if (i < cnt) break;
-                    i -= cnt;
-                    ++gr;
-                }
-                const uint32_t rk = g0 + gr;
-                c[gg] = rk == crank ? win[i] : dsmem_ld64(dsmem_addr(win, rk) + 8u * i);
-            }
-#pragma unroll
-            for (int gg = 0; gg < G; ++gg) {
-                if (i0 + (uint32_t)(gg * THREADS) >= n_lists) continue;
-                const uint32_t f = fine_bin((uint32_t)(c[gg] >> 32), f_lo, sh);
-                const uint32_t o = offs[f];
-                if (o >= pos_lo && o < pos_hi) {
-                    const uint32_t li = atomicAdd(&cur[f], 1u) - pos_lo;
-                    loc[li] = c[gg];
-                    lb = min(lb, li);
-                    le = max(le, li + 1u);
-                }
-            }
-        }
-        lb = __reduce_min_sync(kFull, lb);
-        le = __reduce_max_sync(kFull, le);
-        if (lane == 0 && le > 0) {
-            atomicMin(&ctrl.loc_begin, lb);
-            atomicMax(&ctrl.loc_end, le);
-        }
-        __syncthreads();
-        // A bin's members sit together at [offs - pos_lo, cur - pos_lo); a
-        // member's place is the bin's first place plus the members above it.
-        const uint32_t loc_end = ctrl.loc_end;
-        for (uint32_t i = ctrl.loc_begin + (uint32_t)tid; i < loc_end; i += THREADS) {
-            const uint64_t x = loc[i];
-            const uint32_t e = (uint32_t)(x >> 32);
-            const uint32_t f = fine_bin(e, f_lo, sh);
-            const uint32_t st = offs[f] - pos_lo, en = cur[f] - pos_lo;
-            uint32_t rank = 0;
-            for (uint32_t y = st; y < en; ++y) rank += loc[y] > x;
-            const uint32_t pos = offs[f] + rank;
-            if (pos < n_out) put_out(oi, ov, pos, idx_offset, (int32_t)(~(uint32_t)x), e, excl);
-        }
-        if (leader) pad_out(oi, ov, (int)k_eff, p.k);
-    } else if (tid < (int)csize) {
-        dsmem_st(dsmem_addr(&ctrl.cl_fb, (uint32_t)tid), 1u);   // the cluster runs the full select below
-    }
-    cluster_sync();   // F1: the group's lists are read; every fallback flag is set
-    const bool cluster_fallback = ctrl.cl_fb != 0u;
-    if (fast && leader && p.page_table) page_map_row(p, row, oi, (int)k_eff);
-    if (!cluster_fallback) return;
-
-    // ---- 6. the full radix select, for the groups whose checks failed;
-    //         every CTA of the cluster runs the same cluster barriers ------ //
-    const bool work = !fast;
     if (work) {
         for (int b = tid; b < 2 * kBins; b += THREADS) hist0[b] = 0u;
         if (tid == 0) {
@@ -2703,6 +2579,394 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
         }
     }
     cluster_wait();
+}
+
+template <int THREADS>
+__global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kernel(const Params p)
+{
+    grid_dependency_enter();
+    constexpr uint32_t kZeroKey = 0x80000000u;   // order key of +0.0
+    constexpr uint32_t kZeroDigit = kZeroKey >> 21;
+    constexpr uint32_t kChunk = 32768;           // bytes per bulk copy
+    extern __shared__ __align__(16) unsigned char smem[];
+    CCtrl &ctrl = *reinterpret_cast<CCtrl *>(smem);
+    uint32_t *hist0 = reinterpret_cast<uint32_t *>(smem + sizeof(CCtrl));   // levels 0 and 2
+    uint64_t *win = reinterpret_cast<uint64_t *>(smem + p.off_win);
+    uint32_t *keys = reinterpret_cast<uint32_t *>(smem + p.off_keys);
+    const uint32_t wcap = (uint32_t)p.win_cap;   // candidate list capacity (a power of two)
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t crank = cluster_rank(), csize = cluster_size();
+    const RowGroup g = assign_rows<THREADS>(p, crank, csize, hist0, ctrl.scan);
+    if (g.row < 0) return;   // uniform over the cluster: nothing to select
+    const int row = g.row;
+    const uint32_t g0 = g.g0, gsize = g.gsize, grank = crank - g0;
+    const bool leader = grank == 0;
+
+    // Rows handed out by assign_rows have 0 < L < 2^24 and a valid window.
+    const int64_t rs = g.start;
+    const int32_t L = g.len;
+    const uint32_t k_eff = (uint32_t)(p.k < L ? p.k : L);
+    const int64_t idx_offset = (p.offset_mode & TOPK_OFFSET_ROW_START) ? rs : 0;
+    const bool excl = (p.offset_mode & TOPK_EXCLUDE_NEG_INF) != 0;
+    int32_t *oi = p.out_idx + (int64_t)row * p.k;
+    float *ov = p.out_val ? p.out_val + (int64_t)row * p.k : nullptr;
+
+    Slice s;
+    {
+        const uint64_t pa = (uint64_t)(uintptr_t)p.scores >> 2;   // element address
+        const int64_t e0 = rs, e1 = rs + L;
+        int64_t a0 = e0 + (int64_t)((4u - (uint32_t)((pa + (uint64_t)e0) & 3u)) & 3u);
+        if (a0 > e1) a0 = e1;
+        const int64_t n4 = (e1 - a0) >> 2;
+        // n4 < 2^22 and gsize <= 16: the products fit 32 bits.
+        const int64_t qlo = (uint32_t)n4 * grank / gsize, qhi = (uint32_t)n4 * (grank + 1) / gsize;
+        const int64_t hb = a0 + 4 * qlo, he = a0 + 4 * qhi;
+        const int64_t glo = grank == 0 ? e0 : hb;
+        const int64_t ghi = grank == gsize - 1 ? e1 : he;
+        const int64_t sbase = hb - ((hb - glo + 3) & ~(int64_t)3);
+        s.gptr = p.scores + sbase;
+        s.off0 = (int32_t)(glo - sbase);
+        s.end = (int32_t)(ghi - sbase);
+        s.bq0 = (int32_t)((hb - sbase) >> 2);
+        s.bq1 = (int32_t)((he - sbase) >> 2);
+        s.nq = (s.end + 3) >> 2;
+        s.sq = s.nq < (p.stage_cap >> 2) ? s.nq : (p.stage_cap >> 2);
+        s.jbase = (int32_t)(sbase - rs);
+    }
+    // Each warp's contiguous run of the slice's full quads, with the
+    // partial head quad in warp 0 and the partial tail quad in the last.
+    const Parts ptm = slice_parts<THREADS>(s, warp);
+
+    // ---- 1. the row's sample, then the bulk copies (TMA) of the staged
+    //         body; the sample and the partial head and tail quads are
+    //         read with plain loads into registers, the sample first so
+    //         that it is not queued behind the copies ------------------- //
+    // The sample: the whole row when L <= kSample, else 128 runs of 32
+    // consecutive scores spread evenly over the row (run t starts at
+    // t * (L - 32) / 127), so that it costs a few cache lines per row rather
+    // than a read of most of the row's DRAM bursts.  The same in every CTA
+    // of the group (raw bits; keys after the barrier).
+    constexpr int SPT = kSample / THREADS;
+    static_assert(kPassQuads == 2, "the append step reads the round's two quads");
+    const uint32_t S = (uint32_t)(L < kSample ? L : kSample);
+    uint32_t skey[SPT];
+#pragma unroll
+    for (int u = 0; u < SPT; ++u) {
+        const uint32_t t = (uint32_t)tid + (uint32_t)(u * THREADS);
+        const uint32_t j = L <= kSample ? t : (t >> 5) * (uint32_t)(L - 32) / 127u + (t & 31u);
+        skey[u] = t < S ? __float_as_uint(__ldg(p.scores + rs + j)) : 0u;
+    }
+    // One mbarrier per 32 KB copy, so that each warp can start on its part
+    // of the slice as soon as the copies under it have landed.
+    const int bq_end = s.bq1 < s.sq ? s.bq1 : s.sq;
+    const uint32_t copy_bytes = bq_end > s.bq0 ? 16u * (uint32_t)(bq_end - s.bq0) : 0u;
+    const uint32_t n_chunks = (copy_bytes + kChunk - 1) / kChunk;   // at most 8 (shared memory < 256 KB)
+    if (tid == 0) {
+        for (uint32_t c = 0; c < n_chunks; ++c) mbar_init(&ctrl.bar[c], 1);
+        for (uint32_t c = 0; c < n_chunks; ++c) {
+            const uint32_t off = c * kChunk, len = copy_bytes - off < kChunk ? copy_bytes - off : kChunk;
+            mbar_arrive_expect_tx(&ctrl.bar[c], len);
+            bulk_load(reinterpret_cast<unsigned char *>(keys + 4 * s.bq0) + off,
+                      reinterpret_cast<const unsigned char *>(s.gptr + 4 * s.bq0) + off, len, &ctrl.bar[c]);
+        }
+    }
+    // Staged quads outside the body: at most one head and one tail quad,
+    // raw bits with 0xFFFFFFFF (order key 0) in the empty slots.
+    const int pq_q = tid < 1 ? 0 : s.nq - 1;
+    const bool pq_mine = tid < 2 && pq_q < s.sq && (pq_q < s.bq0 || pq_q >= s.bq1);
+    uint32_t pq[4] = {kFull, kFull, kFull, kFull};
+    if (pq_mine) {
+        const uint32_t m = quad_mask(s, pq_q);
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            if ((m >> i) & 1u) pq[i] = __float_as_uint(__ldg(s.gptr + 4 * pq_q + i));
+    }
+    // Fine histograms: hist0 and hist1 hold four slots of kFineBins words.
+    // A group of up to four CTAs keeps all of its CTAs' histograms in every
+    // CTA: each counts into its own slot (grank) and writes that slot into
+    // its peers before the cluster barrier.  A larger group counts into
+    // slot 3, which its peers read after the barrier.  Nothing but a CTA's
+    // own counting slot is touched before the barrier, so the peers' writes
+    // cannot race with it.  The sample's histograms use the candidate-list
+    // area, which holds no candidates yet.
+    const bool push_mode = gsize <= 4;
+    uint32_t *fine = hist0;                                    // 4 slots of kFineBins
+    uint32_t *fhist = fine + (push_mode ? grank : 3u) * kFineBins;
+    uint32_t *sh0 = reinterpret_cast<uint32_t *>(win), *sh1 = sh0 + kBins;
+    for (int b = tid; b < kFineBins; b += THREADS) fhist[b] = 0u;
+    for (int b = tid; b < 2 * kBins; b += THREADS) sh0[b] = 0u;
+    if (tid == 0) {
+        ctrl.zeros = 0u;
+        ctrl.win_local = 0u;
+        ctrl.smax = 0u;
+        ctrl.overflow = 0u;
+        ctrl.cl_fb = 0u;
+        ctrl.maxbin = 0u;
+        ctrl.loc_begin = kFull;
+        ctrl.loc_end = 0u;
+    }
+    __syncthreads();
+
+    // ---- 2. the candidate bound: the sample's m-th largest key to 2^10
+    //         keys (m = k when the sample is the whole row), by its top 11
+    //         bits and then its next 11 ------------------------------------ //
+    {
+        uint32_t smx = 0;
+#pragma unroll
+        for (int u = 0; u < SPT; ++u) {
+            if ((uint32_t)tid + (uint32_t)(u * THREADS) < S) {
+                skey[u] = order_key(skey[u]);
+                atomicAdd(&sh0[skey[u] >> 21], 1u);
+                smx = max(smx, skey[u]);
+            }
+        }
+        smx = __reduce_max_sync(kFull, smx);
+        if (lane == 0) atomicMax(&ctrl.smax, smx);
+    }
+    __syncthreads();
+    uint32_t m_s = k_eff;
+    if (L > kSample) {
+        const float q = (float)k_eff / (float)L;
+        const float mu = (float)S * q;
+        const float m = ceilf(mu + 4.0f * sqrtf(mu * (1.0f - q)) + 8.0f);
+        m_s = m < (float)S ? (uint32_t)m : S;
+    }
+    {
+        uint32_t d, gt, c;
+        if (find_bin<THREADS>(sh0, m_s, ctrl.scan, d, gt, c)) {
+            ctrl.sel[0] = d;
+            ctrl.sel[1] = gt;
+        }
+    }
+    __syncthreads();
+    const uint32_t d1 = ctrl.sel[0], gt1 = ctrl.sel[1];
+    // A bound on or below the +0.0 digit makes the candidates the positive
+    // keys, with +0.0 counted apart.
+    const bool plat = d1 <= kZeroDigit;
+    {
+        uint32_t smn = kFull;
+#pragma unroll
+        for (int u = 0; u < SPT; ++u) {
+            if ((uint32_t)tid + (uint32_t)(u * THREADS) >= S) continue;
+            if ((skey[u] >> 21) == d1) atomicAdd(&sh1[(skey[u] >> 10) & 0x7FFu], 1u);
+            if (skey[u] > kZeroKey) smn = min(smn, skey[u]);
+        }
+        smn = __reduce_min_sync(kFull, smn);
+        if (lane == 0) atomicMin(&ctrl.loc_begin, smn);
+    }
+    __syncthreads();
+    if (!plat) {
+        uint32_t d, gt, c;
+        if (find_bin<THREADS>(sh1, m_s - gt1, ctrl.scan, d, gt, c)) ctrl.sel[2] = d;
+        __syncthreads();
+    }
+    // Candidates are the keys >= lo; fine bins start at f_lo (the smallest
+    // sampled positive key on the plateau path) and the sample's range
+    // spans 512 of them.
+    const uint32_t lo = plat ? kZeroKey + 1u : (d1 << 21) | (ctrl.sel[2] << 10);
+    const uint32_t f_lo = plat ? (ctrl.loc_begin != kFull ? ctrl.loc_begin : lo) : lo;
+    const uint32_t smax = ctrl.smax;
+    const int span_bits = 32 - __clz(smax > f_lo ? smax - f_lo : 0u);
+    const uint32_t sh = span_bits > 9 ? (uint32_t)(span_bits - 9) : 0u;
+    if (pq_mine) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) keys[4 * pq_q + i] = pq[i];
+    }
+    __syncthreads();   // the partial quads are staged; every thread has read ctrl.loc_begin and ctrl.sel
+
+    // ---- 3. one pass: candidates to the fine histogram and the list ------ //
+    // Slices of up to kMaskRounds rounds per lane take the two-phase pass,
+    // which also writes the composites and the fine histogram; longer ones
+    // the appending pass, finished below.
+    const int mask_r = mask_rounds<THREADS>(s);
+    const uint32_t wcap_eff = wcap;
+    if (mask_r <= kMaskRounds) {
+        if (s.sq == s.nq) {
+            if (plat) masked_pass<THREADS, true, true>(ctrl, s, keys, ptm, win, wcap, mask_r, lo, fhist, f_lo, sh, bq_end);
+            else masked_pass<THREADS, false, true>(ctrl, s, keys, ptm, win, wcap, mask_r, lo, fhist, f_lo, sh, bq_end);
+        } else {
+            if (plat) masked_pass<THREADS, true, false>(ctrl, s, keys, ptm, win, wcap, mask_r, lo, fhist, f_lo, sh, bq_end);
+            else masked_pass<THREADS, false, false>(ctrl, s, keys, ptm, win, wcap, mask_r, lo, fhist, f_lo, sh, bq_end);
+        }
+        __syncthreads();
+    } else {
+        if (plat) sampled_pass<THREADS, true>(ctrl, s, keys, ptm, win, wcap, lo, bq_end);
+        else sampled_pass<THREADS, false>(ctrl, s, keys, ptm, win, wcap, lo, bq_end);
+        __syncthreads();
+        finish_candidates<THREADS>(win, min(ctrl.win_local, wcap), fhist, f_lo, sh);
+    }
+    if (tid == 0) ctrl.loc_begin = kFull;
+    __syncthreads();
+
+    // ---- 4. counters (and, for small groups, the fine histogram) into
+    //         every CTA of the group ---------------------------------------- //
+    if (tid < (int)gsize) {
+        const uint32_t dst = g0 + (uint32_t)tid;
+        const uint32_t v[3] = {ctrl.win_local, ctrl.overflow, ctrl.zeros};
+        uint32_t *fld[3] = {&ctrl.gcnt[grank], &ctrl.gover[grank], &ctrl.gzero[grank]};
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+            if (dst == crank) *fld[i] = v[i];
+            else dsmem_st(dsmem_addr(fld[i], dst), v[i]);
+        }
+    }
+    if (push_mode) {
+        for (uint32_t r0 = g0; r0 < g0 + gsize; ++r0) {
+            if (r0 == crank) continue;
+            for (int b = tid; b < kFineBins; b += THREADS) dsmem_st(dsmem_addr(&fhist[b], r0), fhist[b]);
+        }
+    }
+    cluster_sync();   // F0: every CTA's list, counters and fine histogram are in place
+
+    // ---- 5. the group's totals, every fine bin's first output place ------ //
+    uint32_t n_all = 0, z_all = 0, z_before = 0, over_any = 0;
+    for (uint32_t gr = 0; gr < gsize; ++gr) {
+        n_all += ctrl.gcnt[gr];
+        z_all += ctrl.gzero[gr];
+        z_before += gr < grank ? ctrl.gzero[gr] : 0u;
+        over_any |= ctrl.gover[gr];
+    }
+    // The output places the sampled path fills: all k_eff, or on the
+    // plateau path with fewer positives than k_eff the positives (the first
+    // +0.0 entries follow them).
+    uint32_t n_out = k_eff, r_ties = 0;
+    bool fast = over_any == 0u;
+    if (n_all < k_eff) {
+        if (plat && n_all + z_all >= k_eff) {
+            n_out = n_all;
+            r_ties = k_eff - n_all;
+        } else {
+            fast = false;
+        }
+    }
+    const uint32_t pos_lo = n_out * grank / gsize;   // n_out <= 4096, gsize <= 16: products fit 32 bits
+    const uint32_t pos_hi = n_out * (grank + 1) / gsize;
+    if (tid <= (int)gsize) ctrl.gpos[tid] = n_out * (uint32_t)tid / gsize;
+    constexpr int FB = kFineBins / THREADS;
+    const int flo = kFineBins - (tid + 1) * FB;   // thread 0 owns the top bins
+    uint32_t *offs = fine;                        // slot 0: first output place of each bin
+    uint32_t *base = fine + kFineBins;            // slot 1: the bin's members in lower CTAs
+    uint32_t *lcur = fine + 2 * kFineBins;        // slot 2: this CTA's members placed so far
+    {
+        uint32_t h[FB], hb[FB];
+#pragma unroll
+        for (int i = 0; i < FB; ++i) {
+            h[i] = 0u;
+            hb[i] = 0u;
+        }
+        for (uint32_t gr = 0; gr < gsize; ++gr) {
+#pragma unroll
+            for (int i = 0; i < FB; ++i) {
+                uint32_t v;
+                if (push_mode) v = fine[gr * kFineBins + flo + i];
+                else v = g0 + gr == crank ? fhist[flo + i] : dsmem_ld(dsmem_addr(&fhist[flo + i], g0 + gr));
+                h[i] += v;
+                hb[i] += gr < grank ? v : 0u;
+            }
+        }
+        uint32_t hs = 0, hmax = 0;
+#pragma unroll
+        for (int i = 0; i < FB; ++i) {
+            hs += h[i];
+            hmax = max(hmax, h[i]);
+        }
+        hmax = __reduce_max_sync(kFull, hmax);
+        if (lane == 0) atomicMax(&ctrl.maxbin, hmax);
+        uint32_t run = block_incl_scan<THREADS>(hs, ctrl.scan) - hs;
+        // Every thread rewrites only its own bins of slots 0-2, whose
+        // pushed counts it has read above.
+        uint32_t lb = kFull, le = 0;
+#pragma unroll
+        for (int i = FB - 1; i >= 0; --i) {
+            offs[flo + i] = run;
+            base[flo + i] = hb[i];
+            lcur[flo + i] = 0u;
+            if (h[i] > 0 && run >= pos_lo && run < pos_hi && run < n_out) {
+                lb = min(lb, run - pos_lo);
+                le = max(le, run + h[i] - pos_lo);
+            }
+            run += h[i];
+        }
+        lb = __reduce_min_sync(kFull, lb);
+        le = __reduce_max_sync(kFull, le);
+        if (lane == 0 && le > 0) {
+            atomicMin(&ctrl.loc_begin, lb);
+            atomicMax(&ctrl.loc_end, le);
+        }
+    }
+    const uint32_t n_bins_total = ctrl.scan[THREADS / 32 - 1];
+    __syncthreads();
+    // With no list overflow every candidate was counted once (an overflow
+    // leaves the rest uncounted and sends the group to the full select).
+    if (over_any == 0u && n_all != n_bins_total && tid == 0) atomicOr(&g_status, TOPK_DEV_INTERNAL);
+    const uint32_t loc_cap = (uint32_t)p.stage_cap / 2u;   // composites the staging area holds
+    fast = fast && n_all == n_bins_total && n_all <= loc_cap && ctrl.maxbin <= kMaxFineBin;
+
+    // ---- 6. sampled path: every candidate to the CTA owning its bin's
+    //         first place, at its bin's place range ------------------------ //
+    uint64_t *loc = reinterpret_cast<uint64_t *>(keys);   // the staged slice becomes the gather buffer
+    // A row of one CTA places its first +0.0 entries now, from the staged
+    // slice (no peer writes into this CTA); a larger group does it after F1
+    // from the scores where they lie, since its peers' candidates land in the
+    // staging area.
+    const bool ties_now = fast && r_ties > 0 && gsize == 1;
+    if (ties_now) {
+        write_zero_ties<THREADS>(ctrl, s, keys, ptm, z_before, r_ties, n_out, k_eff, idx_offset, oi, ov, excl);
+        __syncthreads();   // the slice has been read
+    }
+    if (fast) {
+        const uint32_t cnt = min(ctrl.win_local, wcap_eff);
+        for (uint32_t i = (uint32_t)tid; i < cnt; i += THREADS) {
+            const uint64_t c = win[i];
+            const uint32_t f = fine_bin((uint32_t)(c >> 32), f_lo, sh);
+            const uint32_t o = offs[f];
+            if (o >= n_out) continue;   // the bin starts past the output
+            uint32_t gr = 0;
+            while (gr + 1 < gsize && ctrl.gpos[gr + 1] <= o) ++gr;
+            const uint32_t slot = o + base[f] + atomicAdd(&lcur[f], 1u);
+            const uint32_t dst = slot - ctrl.gpos[gr];
+            if (gr == grank) loc[dst] = c;
+            else dsmem_st64(dsmem_addr(&loc[dst], g0 + gr), c);
+        }
+    } else if (tid < (int)csize) {
+        dsmem_st(dsmem_addr(&ctrl.cl_fb, (uint32_t)tid), 1u);   // the cluster runs the full select below
+    }
+    cluster_sync();   // F1: every candidate is with its bin's CTA; every fallback flag is set
+    const bool cluster_fallback = ctrl.cl_fb != 0u;
+    if (fast) {
+        // A bin's members sit together at [offs, offs + count) - pos_lo; a
+        // member's place is the bin's first place plus the members above it.
+        const uint32_t loc_end = ctrl.loc_end;
+        for (uint32_t i = ctrl.loc_begin + (uint32_t)tid; i < loc_end; i += THREADS) {
+            const uint64_t x = loc[i];
+            const uint32_t e = (uint32_t)(x >> 32);
+            const uint32_t f = fine_bin(e, f_lo, sh);
+            const uint32_t st = offs[f] - pos_lo, en = (f > 0 ? offs[f - 1] : n_all) - pos_lo;
+            uint32_t rank = 0;
+            for (uint32_t y = st; y < en; ++y) rank += loc[y] > x;
+            const uint32_t pos = offs[f] + rank;
+            if (pos < n_out) put_out(oi, ov, pos, idx_offset, (int32_t)(~(uint32_t)x), e, excl);
+        }
+        if (r_ties > 0 && !ties_now) {
+            // The first +0.0 entries by index, read where they lie (the
+            // staging area now holds the gathered candidates).
+            Slice sg = s;
+            sg.sq = 0;
+            write_zero_ties<THREADS>(ctrl, sg, keys, ptm, z_before, r_ties, n_out, k_eff, idx_offset, oi, ov, excl);
+        }
+        if (leader) pad_out(oi, ov, (int)k_eff, p.k);
+    }
+    if (p.page_table) {
+        __syncthreads();
+        cluster_sync();   // the group's output writes are done
+        if (fast && leader) page_map_row(p, row, oi, (int)k_eff);
+    }
+    if (!cluster_fallback) return;
+
+    // ---- 7. the full radix select, for the groups whose checks failed;
+    //         every CTA of the cluster runs the same cluster barriers ------ //
+    full_select<THREADS>(p, s, g, !fast);
 }
 
 // ------------------------------------------------------------------------- //

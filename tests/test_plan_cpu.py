@@ -55,13 +55,14 @@ int main()
                     const bool cl = pl.variant != kRowKernel;
                     CHECK(pl.off_win >= header_bytes(cl));
                     CHECK(pl.off_win % 16 == 0);
-                    CHECK(pl.win_cap >= (cl ? 2 * k : k - 1));
+                    CHECK(pl.win_cap >= (cl ? (2 * k > 2048 ? 2 * k : 2048) : k - 1));
                     CHECK((pl.win_cap & (pl.win_cap - 1)) == 0);
                     CHECK(pl.off_keys % 128 == 0);
                     CHECK(pl.off_keys >= pl.off_win + 8 * pl.win_cap);
                     CHECK(pl.stage_cap % 128 == 0 && pl.stage_cap > 0);
                     CHECK(pl.stage_cap >= 2 * pl.win_cap);
                     CHECK(pl.smem == pl.off_keys + 4 * pl.stage_cap);
+                    CHECK(4 * pl.stage_cap <= 8 * 32768);   // at most eight 32 KB copies per slice
                     CHECK(pl.smem <= dev.max_smem);
                     if (cl) {
                         CHECK(pl.smem <= variant_budget(dev, pl.variant));
