@@ -115,9 +115,8 @@ inline int header_bytes(bool cluster)
 // cluster kernel keeps up to twice k candidates per CTA.
 inline int list_cap(bool cluster, int k)
 {
-    // The cluster kernel's list also holds the two 2048-bin histograms of
-    // the row's sample before the candidates are appended: 2048 slots at
-    // least.
+    // The cluster kernel's list also holds the 4096-bin histogram of the
+    // row's sample before the candidates are appended: 2048 slots at least.
     return cluster ? (2 * next_pow2(k) > 2048 ? 2 * next_pow2(k) : 2048) : next_pow2(k - 1 > 1 ? k - 1 : 1);
 }
 

@@ -399,6 +399,41 @@ __device__ __forceinline__ bool find_bin(const uint32_t *h, uint32_t r, uint32_t
     return mine;
 }
 
+// find_bin over NB bins (NB / THREADS a multiple of 2 per thread).
+template <int THREADS, int NB>
+__device__ __forceinline__ bool find_bin_nb(const uint32_t *h, uint32_t r, uint32_t *sm, uint32_t &digit,
+                                            uint32_t &gt)
+{
+    constexpr int BPT = NB / THREADS;
+    static_assert(BPT % 2 == 0, "two or more bins per thread");
+    const int lo = NB - ((int)threadIdx.x + 1) * BPT;   // thread 0 owns the top bins
+    uint32_t v[BPT];
+#pragma unroll
+    for (int i = 0; i < BPT; i += 2) {
+        const uint2 x = *reinterpret_cast<const uint2 *>(h + lo + i);
+        v[i] = x.x;
+        v[i + 1] = x.y;
+    }
+    uint32_t sum = 0;
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) sum += v[i];
+    const uint32_t incl = block_incl_scan<THREADS>(sum, sm);
+    bool mine = false;
+    if (incl - sum < r && r <= incl) {
+        uint32_t acc = incl - sum;
+#pragma unroll
+        for (int i = BPT - 1; i >= 0; --i) {
+            if (!mine && acc + v[i] >= r) {
+                mine = true;
+                digit = (uint32_t)(lo + i);
+                gt = acc;
+            }
+            acc += v[i];
+        }
+    }
+    return mine;
+}
+
 __device__ __forceinline__ uint32_t lanemask_lt()
 {
     uint32_t m;
@@ -881,24 +916,70 @@ __device__ RowGroup assign_rows(const Params &p, uint32_t crank, uint32_t csize,
     uint32_t *eff = scratch;              // B valid lengths (0: nothing to select)
     uint32_t *starts = scratch + 512;     // B row starts
     uint32_t *by_rank = scratch + 1024;   // row index of every rank
-    for (int i = tid; i < B; i += THREADS) {
-        int64_t len;
-        eff[i] = row_window_ok(p, i, len) ? (uint32_t)len : 0u;
-        starts[i] = (uint32_t)p.row_starts[i];
-    }
-    for (int i = B + tid; i < ((B + 3) & ~3); i += THREADS) eff[i] = 0u;   // pad to whole vectors
-    __syncthreads();
-    for (int i = tid; i < B; i += THREADS) {
-        const uint32_t e = eff[i];
-        int rank = 0;
-        for (int j = 0; j < B; j += 4) {
-            const uint4 q = *reinterpret_cast<const uint4 *>(eff + j);
-            rank += (q.x > e || (q.x == e && j < i)) + (q.y > e || (q.y == e && j + 1 < i)) +
-                    (q.z > e || (q.z == e && j + 2 < i)) + (q.w > e || (q.w == e && j + 3 < i));
+    if (B <= 64) {
+        // Up to 64 rows: warp 0 alone loads them (rows lane and lane + 32)
+        // and ranks them with a bitonic sort of (length << 6 | 63 - row),
+        // descending: length descending, row ascending.
+        if (tid < 32) {
+            const int lane = tid;
+            uint32_t a[2];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+                const int i = lane + 32 * h;
+                a[h] = 0u;
+                if (i < B) {
+                    int64_t len;
+                    const uint32_t e = row_window_ok(p, i, len) ? (uint32_t)len : 0u;
+                    eff[i] = e;
+                    starts[i] = (uint32_t)p.row_starts[i];
+                    a[h] = (e << 6) | (uint32_t)(63 - i);
+                }
+            }
+#pragma unroll
+            for (int k = 2; k <= 64; k <<= 1) {
+#pragma unroll
+                for (int j = k >> 1; j > 0; j >>= 1) {
+                    if (j == 32) {   // elements lane and lane + 32, in one lane
+                        const uint32_t hi = max(a[0], a[1]), lo = min(a[0], a[1]);
+                        a[0] = hi;
+                        a[1] = lo;
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const int i = lane + 32 * h;
+                            const uint32_t o = __shfl_xor_sync(kFull, a[h], j);
+                            // Blocks with (i & k) == 0 run descending.
+                            const bool keep_max = ((i & j) == 0) == ((i & k) == 0);
+                            a[h] = keep_max ? max(a[h], o) : min(a[h], o);
+                        }
+                    }
+                }
+            }
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+                if (lane + 32 * h < B) by_rank[lane + 32 * h] = 63u - (a[h] & 63u);
+            __syncwarp();
         }
-        by_rank[rank] = (uint32_t)i;
+    } else {
+        for (int i = tid; i < B; i += THREADS) {
+            int64_t len;
+            eff[i] = row_window_ok(p, i, len) ? (uint32_t)len : 0u;
+            starts[i] = (uint32_t)p.row_starts[i];
+        }
+        for (int i = B + tid; i < ((B + 3) & ~3); i += THREADS) eff[i] = 0u;   // pad to whole vectors
+        __syncthreads();
+        for (int i = tid; i < B; i += THREADS) {
+            const uint32_t e = eff[i];
+            int rank = 0;
+            for (int j = 0; j < B; j += 4) {
+                const uint4 q = *reinterpret_cast<const uint4 *>(eff + j);
+                rank += (q.x > e || (q.x == e && j < i)) + (q.y > e || (q.y == e && j + 1 < i)) +
+                        (q.z > e || (q.z == e && j + 2 < i)) + (q.w > e || (q.w == e && j + 3 < i));
+            }
+            by_rank[rank] = (uint32_t)i;
+        }
+        __syncthreads();
     }
-    __syncthreads();
     if (tid < 32) {
         // The cluster's rows, one per lane of warp 0, in the order they are
         // dealt: lane i holds rank t_i (the pair of block i / 2), and t_i
@@ -2693,9 +2774,9 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
     const bool push_mode = gsize <= 4;
     uint32_t *fine = hist0;                                    // 4 slots of kFineBins
     uint32_t *fhist = fine + (push_mode ? grank : 3u) * kFineBins;
-    uint32_t *sh0 = reinterpret_cast<uint32_t *>(win), *sh1 = sh0 + kBins;
+    uint32_t *sh0 = reinterpret_cast<uint32_t *>(win);   // 4096 bins (the list holds at least 2048 composites)
     for (int b = tid; b < kFineBins; b += THREADS) fhist[b] = 0u;
-    for (int b = tid; b < 2 * kBins; b += THREADS) sh0[b] = 0u;
+    for (int b = tid; b < 4096; b += THREADS) sh0[b] = 0u;
     if (tid == 0) {
         ctrl.zeros = 0u;
         ctrl.win_local = 0u;
@@ -2708,21 +2789,27 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
     }
     __syncthreads();
 
-    // ---- 2. the candidate bound: the sample's m-th largest key to 2^10
-    //         keys (m = k when the sample is the whole row), by its top 11
-    //         bits and then its next 11 ------------------------------------ //
+    // ---- 2. the candidate bound: the top 12 bits (an eighth of a binade)
+    //         of the sample's m-th largest key (m = k when the sample is the
+    //         whole row), from a 4096-bin histogram of the sample ----------- //
+    constexpr int kSampleBins = 4096;
     {
-        uint32_t smx = 0;
+        uint32_t smx = 0, smn = kFull;
 #pragma unroll
         for (int u = 0; u < SPT; ++u) {
             if ((uint32_t)tid + (uint32_t)(u * THREADS) < S) {
                 skey[u] = order_key(skey[u]);
-                atomicAdd(&sh0[skey[u] >> 21], 1u);
+                atomicAdd(&sh0[skey[u] >> 20], 1u);
                 smx = max(smx, skey[u]);
+                if (skey[u] > kZeroKey) smn = min(smn, skey[u]);
             }
         }
         smx = __reduce_max_sync(kFull, smx);
-        if (lane == 0) atomicMax(&ctrl.smax, smx);
+        smn = __reduce_min_sync(kFull, smn);
+        if (lane == 0) {
+            atomicMax(&ctrl.smax, smx);
+            atomicMin(&ctrl.loc_begin, smn);   // loc_begin is free until the gather
+        }
     }
     __syncthreads();
     uint32_t m_s = k_eff;
@@ -2733,38 +2820,17 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
         m_s = m < (float)S ? (uint32_t)m : S;
     }
     {
-        uint32_t d, gt, c;
-        if (find_bin<THREADS>(sh0, m_s, ctrl.scan, d, gt, c)) {
-            ctrl.sel[0] = d;
-            ctrl.sel[1] = gt;
-        }
+        uint32_t d, gt;
+        if (find_bin_nb<THREADS, kSampleBins>(sh0, m_s, ctrl.scan, d, gt)) ctrl.sel[0] = d;
     }
     __syncthreads();
-    const uint32_t d1 = ctrl.sel[0], gt1 = ctrl.sel[1];
     // A bound on or below the +0.0 digit makes the candidates the positive
-    // keys, with +0.0 counted apart.
-    const bool plat = d1 <= kZeroDigit;
-    {
-        uint32_t smn = kFull;
-#pragma unroll
-        for (int u = 0; u < SPT; ++u) {
-            if ((uint32_t)tid + (uint32_t)(u * THREADS) >= S) continue;
-            if ((skey[u] >> 21) == d1) atomicAdd(&sh1[(skey[u] >> 10) & 0x7FFu], 1u);
-            if (skey[u] > kZeroKey) smn = min(smn, skey[u]);
-        }
-        smn = __reduce_min_sync(kFull, smn);
-        if (lane == 0) atomicMin(&ctrl.loc_begin, smn);
-    }
-    __syncthreads();
-    if (!plat) {
-        uint32_t d, gt, c;
-        if (find_bin<THREADS>(sh1, m_s - gt1, ctrl.scan, d, gt, c)) ctrl.sel[2] = d;
-        __syncthreads();
-    }
-    // Candidates are the keys >= lo; fine bins start at f_lo (the smallest
-    // sampled positive key on the plateau path) and the sample's range
-    // spans 512 of them.
-    const uint32_t lo = plat ? kZeroKey + 1u : (d1 << 21) | (ctrl.sel[2] << 10);
+    // keys, with +0.0 counted apart.  Candidates are the keys >= lo; fine
+    // bins start at f_lo (the smallest sampled positive key on the plateau
+    // path) and the sample's range spans 512 of them.
+    const uint32_t d1 = ctrl.sel[0];
+    const bool plat = d1 <= (kZeroKey >> 20);
+    const uint32_t lo = plat ? kZeroKey + 1u : d1 << 20;
     const uint32_t f_lo = plat ? (ctrl.loc_begin != kFull ? ctrl.loc_begin : lo) : lo;
     const uint32_t smax = ctrl.smax;
     const int span_bits = 32 - __clz(smax > f_lo ? smax - f_lo : 0u);
