@@ -37,13 +37,11 @@ struct alignas(16) Ctrl {
     uint32_t warp_ties[32];
     uint32_t scan[36];
     uint64_t scan64[32];
-    // Short-row path: per-warp partials (entries above +0.0, +0.0 count,
-    // smallest and largest non-zero key) and the bucket statistics.
-    uint32_t part_p[32], part_z[32], part_min[32], part_max[32];
-    uint32_t sq;         // sum of squared sizes of the buckets that are output
+    // Short-row path: per-warp partials (non-zero count, smallest and
+    // largest non-zero key) and the bucket statistics.
+    uint32_t part_p[32], part_min[32], part_max[32];
+    uint32_t sq;         // the largest bucket among those that are output
     uint32_t npart;      // entries in those buckets
-    uint32_t tot_p;      // entries above +0.0
-    uint32_t tot_z;      // +0.0 entries
 };
 
 // Per-CTA control block of the cluster kernel.

@@ -286,13 +286,31 @@ __device__ __forceinline__ uint32_t block_incl_scan(uint32_t x, uint32_t *sm)
     return x;
 }
 
-// Histogram increment.  On this GPU a shared-memory atomic add whose lanes
-// collide on one address is merged by the hardware at full rate, while
-// __match_any_sync is serialised per distinct value, so the plain per-lane
-// atomic is the cheapest form on every digit distribution, plateau included.
+// Histogram increment: one shared-memory atomic add of 1 per lane.  The build
+// switch TOPK_MATCH_AGGREGATE=1 (off in the library, kept for the measured
+// comparison) merges the lanes of a warp that hit one bin with
+// __match_any_sync first and lets one of them add the group's count; on the
+// decode and causal prefill batches that form was slower (the plain atomic
+// is merged by the shared-memory unit, the match costs a warp-wide
+// instruction per increment).
+#ifndef TOPK_MATCH_AGGREGATE
+#define TOPK_MATCH_AGGREGATE 0
+#endif
+__device__ __forceinline__ void hist_inc(uint32_t *hist, uint32_t bin)
+{
+#if TOPK_MATCH_AGGREGATE
+    uint32_t lt;
+    asm("mov.u32 %0, %%lanemask_lt;" : "=r"(lt));
+    const uint32_t peers = __match_any_sync(__activemask(), bin);
+    if ((peers & lt) == 0u) atomicAdd(&hist[bin], (uint32_t)__popc(peers));
+#else
+    atomicAdd(&hist[bin], 1u);
+#endif
+}
+
 __device__ __forceinline__ void hist_add(uint32_t *hist, uint32_t digit, bool valid)
 {
-    if (valid) atomicAdd(&hist[digit], 1u);
+    if (valid) hist_inc(hist, digit);
 }
 
 // ------------------------------------------------------------------------- //
@@ -520,7 +538,7 @@ __device__ void sort_and_write(uint64_t *a, uint64_t *b, int n, int n_out, int c
     const int s = max(0, (32 - __clz(range)) - 11);
     for (int i = tid; i < kBins; i += THREADS) cur[i] = 0u;
     __syncthreads();
-    for (int i = tid; i < n; i += THREADS) atomicAdd(&cur[((uint32_t)(a[i] >> 32) - kmin) >> s], 1u);
+    for (int i = tid; i < n; i += THREADS) hist_inc(cur, ((uint32_t)(a[i] >> 32) - kmin) >> s);
     __syncthreads();
     const int lo = kBins - (tid + 1) * BPT;
     uint32_t v[BPT];
@@ -572,12 +590,67 @@ __device__ void sort_and_write(uint64_t *a, uint64_t *b, int n, int n_out, int c
     }
 }
 
+// ------------------------------------------------------------------------- //
+// Short rows: one CTA per row with the whole row in registers (at most
+// kShortQuads quads per thread).  Canonical order cuts a row at the order
+// key of +0.0 into P (keys above it), the +0.0 entries and N (keys below
+// it), and lists P in key order, then the +0.0 entries by index, then N in
+// key order.  The non-zero entries are ranked together by one bucket pass
+// over their own key range [kmin, kmax]: 2^nb buckets of 2^sh keys, about
+// four per non-zero entry, bucket starts from a scan, every entry dropped
+// into its bucket, and its place the bucket start plus the number of
+// members of its bucket above it (composites are unique, so this is exact).
+// When the row holds both signs, the bucket grid is shifted so that a bucket
+// edge falls on +0.0's key: the start of the first bucket below it is then
+// |P|.  Buckets that start at or after k are never output and are not
+// ranked.  An N entry moves down by the +0.0 count; a +0.0 entry's place is
+// |P| plus its ordinal in index order, from per-warp ballots.  When an
+// output bucket is too big for member counting to stay cheap (heavy ties off
+// +0.0) the function returns false with shared memory released and the
+// general path runs.
+//
+// The counters are one 32-bit word per bucket (at most 4096 buckets), each
+// histogram atomic a constant +1.
+// ------------------------------------------------------------------------- //
+constexpr int kShortMinWordsLog = 10;        // at least 1024 counter words
+constexpr int kShortMaxWordsLog = 12;        // at most 4096 counter words (16 KB)
+constexpr int kShortExtraBits = 2;           // about four buckets per non-zero entry
+constexpr uint32_t kShortMaxBucket = 48;     // largest output bucket ranked by counting
+// Build switch kept for the measured comparison of counter forms (off in
+// the library): TOPK_SHORT_PACKED=1 packs two 16-bit counters into a word
+// (twice the buckets, a variable increment of 1 or 1 << 16).  On the causal
+// prefill batch (16384 rows, k = 2048) it ran slower than one-word counters
+// with a constant increment.
+#ifndef TOPK_SHORT_PACKED
+#define TOPK_SHORT_PACKED 0
+#endif
+constexpr bool kShortPacked = TOPK_SHORT_PACKED;
+
+// One quad of a short row as order keys, every slot outside the row read as
+// the key of +0.0 (its bit in m is clear).
+__device__ __forceinline__ uint4 load_quad_short(const Slice &s, int q, uint32_t &m)
+{
+    constexpr uint32_t kZ = 0x80000000u;
+    if (q >= s.bq0 && q < s.bq1) {
+        const float4 f = __ldg(reinterpret_cast<const float4 *>(s.gptr) + q);
+        m = 0xFu;
+        return make_uint4(order_key(__float_as_uint(f.x)), order_key(__float_as_uint(f.y)),
+                          order_key(__float_as_uint(f.z)), order_key(__float_as_uint(f.w)));
+    }
+    m = q < s.nq ? quad_mask(s, q) : 0u;
+    uint32_t e[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+        e[i] = ((m >> i) & 1u) ? order_key(__float_as_uint(__ldg(s.gptr + 4 * q + i))) : kZ;
+    return make_uint4(e[0], e[1], e[2], e[3]);
+}
+
+// Entries k_eff .. k of an output row as -1 (and -inf), 16-byte stores over
+// the aligned middle.
 __device__ __forceinline__ void pad_out(int32_t *oi, float *ov, int from, int to)
 {
     if (from >= to) return;
     const int t = (int)threadIdx.x, nt = (int)blockDim.x;
-    // Indices: 16-byte stores over the aligned middle, single stores over
-    // the (fewer than four) entries before and after it.
     int a = from + (int)((4u - (uint32_t)(((uintptr_t)(oi + from) >> 2) & 3u)) & 3u);
     if (a > to) a = to;
     const int nv = (to - a) >> 2, tail = a + 4 * nv;
@@ -589,34 +662,43 @@ __device__ __forceinline__ void pad_out(int32_t *oi, float *ov, int from, int to
         for (int p = from + t; p < to; p += nt) ov[p] = __uint_as_float(kNegInfBits);
 }
 
-// ------------------------------------------------------------------------- //
-// Short rows: one CTA per row with the whole row in registers (at most
-// kShortQuads quads per thread).  Canonical order cuts a row at the order
-// key of +0.0 into P (keys above it), the +0.0 entries and N (keys below
-// it), and lists P in key order, then the +0.0 entries by index, then N in
-// key order.  The non-zero entries are ranked together by one bucket pass
-// over their own key range: 2 x kBins buckets of 2^sh keys (16-bit counters, two
-// to a word), bucket starts from a
-// scan, every entry dropped into its bucket, and its place the bucket start
-// plus the number of members of its bucket above it (composites are unique,
-// so this is exact).  Buckets that start at or after k are never output and
-// are not ranked.  An N entry moves down by the +0.0 count; a +0.0 entry's
-// place is |P| plus its ordinal in index order, from per-warp ballots.  So a
-// row costs one read, two shared-memory atomics per non-zero entry and no
-// radix levels.  When the output buckets are too big for member counting to
-// stay cheap (heavy ties off +0.0) or overflow the scratch, the function
-// returns false with shared memory released and the general path runs.
-// ------------------------------------------------------------------------- //
-constexpr int kShortBucketBits = 12;   // 2 * kBins buckets with 16-bit counters
-
+// Exclusive scan over the CTA in thread order with one barrier: every warp
+// adds up the totals of the warps before it.  `sm` holds NW words and must
+// not be reused before the next __syncthreads.
 template <int THREADS>
-__device__ bool short_row(Ctrl &ctrl, uint32_t *cur, uint64_t *buf, uint32_t buf_cap, const Slice &s,
-                          uint32_t k_eff, int64_t idx_offset, int32_t *oi, float *ov, int k, bool excl)
+__device__ __forceinline__ uint32_t block_excl_scan1(uint32_t x, uint32_t *sm, uint32_t &total)
 {
     constexpr int NW = THREADS / 32;
-    constexpr int BPT = kBins / THREADS;
+    static_assert(NW % 4 == 0, "warp totals read as 16-byte vectors");
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t incl = warp_incl_scan(x);
+    if (lane == 31) sm[warp] = incl;
+    __syncthreads();
+    uint32_t before = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < NW; w += 4) {
+        const uint4 v = *reinterpret_cast<const uint4 *>(sm + w);
+        before += (w < warp ? v.x : 0u) + (w + 1 < warp ? v.y : 0u) + (w + 2 < warp ? v.z : 0u) +
+                  (w + 3 < warp ? v.w : 0u);
+        all += v.x + v.y + v.z + v.w;
+    }
+    total = all;
+    return before + incl - x;
+}
+
+template <int THREADS>
+__device__ bool short_row(Ctrl &ctrl, unsigned char *area, uint32_t area_bytes, const Slice &s, uint32_t k_eff,
+                          int64_t idx_offset, int32_t *oi, float *ov, int k, bool excl)
+{
+    constexpr int NW = THREADS / 32;
     constexpr uint32_t kZ = 0x80000000u;   // order key of +0.0
+    constexpr bool PK = kShortPacked;
+    constexpr int kMaxWords = 1 << kShortMaxWordsLog;
+    constexpr int kBucketsPerWord = PK ? 2 : 1;
     static_assert(kShortQuads * NW <= 32, "one (quad round, warp) count per lane of warp 0");
+    static_assert((1 << kShortMinWordsLog) % (4 * THREADS) == 0, "whole 16-byte word groups per thread");
+    static_assert(kMaxWords / (4 * THREADS) <= 4, "at most four word groups per thread");
+    uint32_t *cur = reinterpret_cast<uint32_t *>(area);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const uint32_t lt = lanemask_lt();
 
@@ -624,186 +706,256 @@ __device__ bool short_row(Ctrl &ctrl, uint32_t *cur, uint64_t *buf, uint32_t buf
     // warp, then lane, then slot.  Round u of a warp holds data iff
     // active(u); the test is warp-uniform.
     auto active = [&](int u) { return warp * 32 + u * THREADS < s.nq; };
+    for (int i = tid; i < kMaxWords / 4; i += THREADS) reinterpret_cast<uint4 *>(cur)[i] = make_uint4(0, 0, 0, 0);
+    if (tid == 0) ctrl.sq = 0u;
+    // Keys, the 16-bit masks of valid slots (vm) and of +0.0-keyed slots
+    // (zm: the +0.0 entries and every slot outside the row), the range of
+    // the non-zero keys, and the +0.0 count of each round (8 bits a round).
     uint32_t key[kShortQuads][4];
-    uint32_t vm[kShortQuads];
+    uint32_t zm = 0, vm = 0, kmin = kFull, kmax = 0, zc = 0;
 #pragma unroll
     for (int u = 0; u < kShortQuads; ++u) {
-        const int q = tid + u * THREADS;
-        vm[u] = 0;
-        uint4 kk = make_uint4(0, 0, 0, 0);
-        if (q < s.nq) kk = load_quad_global(s, q, vm[u]);
-        key[u][0] = kk.x; key[u][1] = kk.y; key[u][2] = kk.z; key[u][3] = kk.w;
-    }
-    for (int b = tid; b < kBins; b += THREADS) cur[b] = 0u;
-    if (tid == 0) {
-        ctrl.sq = 0u;
-        ctrl.npart = 0u;
-    }
-    // Per round: the +0.0 slots (zm, 4 bits a round) and the non-zero slots
-    // (nm); their per-warp +0.0 counts in index order go to warp_zeros.
-    uint32_t zm = 0, nm = 0, pc = 0, kmin = kFull, kmax = 0;
-#pragma unroll
-    for (int u = 0; u < kShortQuads; ++u) {
+        key[u][0] = key[u][1] = key[u][2] = key[u][3] = kZ;
         if (!active(u)) continue;
-        uint32_t z = 0, n = 0;
+        uint32_t m;
+        const uint4 kk = load_quad_short(s, tid + u * THREADS, m);
+        key[u][0] = kk.x; key[u][1] = kk.y; key[u][2] = kk.z; key[u][3] = kk.w;
+        uint32_t z4 = 0;
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             const uint32_t e = key[u][i];
-            const bool v = (vm[u] >> i) & 1u;
-            z |= (uint32_t)(v && e == kZ) << i;
-            n |= (uint32_t)(v && e != kZ) << i;
-            pc += v && e > kZ;
-            if (v && e != kZ) {
-                kmin = min(kmin, e);
-                kmax = max(kmax, e);
-            }
+            const bool z = e == kZ;
+            z4 |= (uint32_t)z << i;
+            kmin = min(kmin, z ? kFull : e);
+            kmax = max(kmax, z ? 0u : e);
         }
-        zm |= z << (4 * u);
-        nm |= n << (4 * u);
-        const uint32_t zw = __reduce_add_sync(kFull, (uint32_t)__popc(z));
-        if (lane == 0) ctrl.warp_zeros[u * NW + warp] = zw;
+        zm |= z4 << (4 * u);
+        vm |= m << (4 * u);
+        zc |= (uint32_t)__popc(z4 & m) << (8 * u);
     }
-    pc = __reduce_add_sync(kFull, pc);
+    const uint32_t nzm = vm & ~zm;   // non-zero entries
     kmin = __reduce_min_sync(kFull, kmin);
     kmax = __reduce_max_sync(kFull, kmax);
+    const uint32_t nnz_w = __reduce_add_sync(kFull, (uint32_t)__popc(nzm));
+    zc = __reduce_add_sync(kFull, zc);   // at most 128 a round: no carry between rounds
     if (lane == 0) {
-        ctrl.part_p[warp] = pc;
         ctrl.part_min[warp] = kmin;
         ctrl.part_max[warp] = kmax;
+        ctrl.part_p[warp] = nnz_w;
     }
-    if (lane < kShortQuads && !active(lane)) ctrl.warp_zeros[lane * NW + warp] = 0u;
+    if (lane < kShortQuads) ctrl.warp_zeros[lane * NW + warp] = (zc >> (8 * lane)) & 0xFFu;
     __syncthreads();
 
-    uint32_t nzmin = kFull, nzmax = 0;
+    uint32_t nzmin = kFull, nzmax = 0, nnz = 0;
 #pragma unroll
     for (int w = 0; w < NW; w += 4) {
         const uint4 a = *reinterpret_cast<const uint4 *>(&ctrl.part_min[w]);
         const uint4 b = *reinterpret_cast<const uint4 *>(&ctrl.part_max[w]);
+        const uint4 c = *reinterpret_cast<const uint4 *>(&ctrl.part_p[w]);
         nzmin = min(min(nzmin, min(a.x, a.y)), min(a.z, a.w));
         nzmax = max(max(nzmax, max(b.x, b.y)), max(b.z, b.w));
+        nnz += c.x + c.y + c.z + c.w;
     }
-    const bool any_nz = nzmin <= nzmax;   // CTA-uniform
-    const int sh = any_nz ? max(0, (32 - __clz(nzmax - nzmin)) - kShortBucketBits) : 0;
-#pragma unroll
-    for (int u = 0; u < kShortQuads; ++u) {
-        if (!active(u) || !__any_sync(kFull, (nm >> (4 * u)) & 0xFu)) continue;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            if ((nm >> (4 * u + i)) & 1u) {
-                const uint32_t d = (key[u][i] - nzmin) >> sh;
-                atomicAdd(&cur[d >> 1], 1u << ((d & 1u) << 4));
-            }
+    if (tid == 0) ctrl.npart = nnz;   // lowered below to the first bucket start at or past k_eff
+    // Bucket grid: 2^nb buckets (nb from the non-zero count, within the
+    // area left beside the composites that are ranked), bucket d holding keys
+    // base + [d << sh, (d + 1) << sh).
+    const uint32_t need = min(nnz, k_eff + kShortMaxBucket);
+    constexpr int kPk = PK ? 1 : 0;
+    int nb = (32 - __clz(max(nnz, 2u) - 1u)) + kShortExtraBits;
+    nb = min(max(nb, kShortMinWordsLog + kPk), kShortMaxWordsLog + kPk);
+    while (nb > kShortMinWordsLog + kPk && (4u << (nb - kPk)) + 8u * need > area_bytes) --nb;
+    const uint32_t nwords = 1u << (nb - kPk);
+    uint64_t *buf = reinterpret_cast<uint64_t *>(area + 4u * nwords);
+    const uint32_t buf_cap = (area_bytes - 4u * nwords) / 8u;
+    int sh = max(0, (32 - __clz(nzmax - nzmin)) - nb);
+    uint32_t base = nzmin, c0 = 0;   // c0: first bucket above +0.0 when the row has both signs
+    const bool split = nnz && nzmin < kZ && nzmax > kZ;
+    if (split) {
+        c0 = (kZ - nzmin + (1u << sh) - 1u) >> sh;
+        base = kZ - (c0 << sh);
+        if ((nzmax - base) >> sh >> nb) {
+            ++sh;
+            c0 = (kZ - nzmin + (1u << sh) - 1u) >> sh;
+            base = kZ - (c0 << sh);
         }
     }
-    if (warp == 0) {
-        // Exclusive bases of the (round, warp) +0.0 counts in index order,
-        // and the row totals.
-        const uint32_t z = lane < kShortQuads * NW ? ctrl.warp_zeros[lane] : 0u;
-        const uint32_t zi = warp_incl_scan(z);
-        if (lane < kShortQuads * NW) ctrl.warp_ties[lane] = zi - z;
-        const uint32_t pp = __reduce_add_sync(kFull, lane < NW ? ctrl.part_p[lane] : 0u);
-        if (lane == 31) {
-            ctrl.tot_z = zi;
-            ctrl.tot_p = pp;
-        }
-    }
-    __syncthreads();
-
-    const uint32_t P = ctrl.tot_p, Zc = ctrl.tot_z;
-    // The +0.0 entries go to P + their ordinal in index order.
-    if (Zc > 0 && P < k_eff) {
+    // Counter word and increment of bucket d.
+    auto word_of = [&](uint32_t d) { return PK ? d >> 1 : d; };
+    auto inc_of = [&](uint32_t d) { return PK ? 1u << ((d & 1u) << 4) : 1u; };
+    if (nnz) {
 #pragma unroll
         for (int u = 0; u < kShortQuads; ++u) {
-            const uint32_t z = (zm >> (4 * u)) & 0xFu;
-            if (!active(u) || !__any_sync(kFull, z)) continue;
-            const int32_t j0 = (int32_t)idx_offset + s.jbase + 4 * (tid + u * THREADS);
-            uint32_t ord = P + ctrl.warp_ties[u * NW + warp];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) ord += (uint32_t)__popc(__ballot_sync(kFull, (z >> i) & 1u) & lt);
+            if (!active(u)) continue;
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                const uint32_t o = ord + (uint32_t)__popc(z & ((1u << i) - 1u));
-                if (((z >> i) & 1u) && o < k_eff) oi[o] = j0 + i;
-            }
-            if (ov) {
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    const uint32_t o = ord + (uint32_t)__popc(z & ((1u << i) - 1u));
-                    if (((z >> i) & 1u) && o < k_eff) ov[o] = 0.0f;
+                if ((nzm >> (4 * u + i)) & 1u) {
+                    const uint32_t d = (key[u][i] - base) >> sh;
+                    if (PK)
+                        atomicAdd(&cur[word_of(d)], inc_of(d));
+                    else
+                        hist_inc(cur, d);
                 }
             }
         }
     }
-    if (any_nz) {
-        // Bucket starts, top bucket first (in a word the high half is the
-        // higher bucket); the buckets that start below k are the ones output.
-        const int lo = kBins - (tid + 1) * BPT;
-        uint32_t v[BPT];
-        load_bins<THREADS>(cur, lo, v);
+    __syncthreads();
+    uint32_t P = 0;
+    if (nnz) {
+        // Bucket starts, top bucket first (in a packed word the high half
+        // is the higher bucket).  Thread t scans nch groups of four words,
+        // thread 0 the top ones; the sums of a word's two halves never carry.
+        const int nch = (int)nwords / (4 * THREADS);
+        const int w0 = (int)nwords - (tid + 1) * 4 * nch;
+        uint4 v[4];
         uint32_t sum = 0;
 #pragma unroll
-        for (int i = 0; i < BPT; ++i) sum += (v[i] >> 16) + (v[i] & 0xFFFFu);
-        uint32_t run = block_incl_scan<THREADS>(sum, ctrl.scan) - sum;
-        uint32_t sq = 0, np = 0;
+        for (int c = 0; c < 4; ++c) {
+            if (c < nch) {
+                v[c] = *reinterpret_cast<const uint4 *>(cur + w0 + 4 * c);
+                sum += v[c].x + v[c].y + v[c].z + v[c].w;
+            }
+        }
+        const uint32_t tot = PK ? (sum >> 16) + (sum & 0xFFFFu) : sum;
+        uint32_t all;
+        const uint32_t run_in = block_excl_scan1<THREADS>(tot, ctrl.scan, all);
+        // np: the first bucket start at or past k_eff in this thread's
+        // words; mx: the largest bucket.
+        uint32_t run = run_in, mx = 0, np = kFull;
+        auto start_of = [&](uint32_t x) {   // word of counts -> word of starts
+            if (PK) {
+                const uint32_t hi = x >> 16, st = run * 0x10001u + hi;
+                const uint32_t lo_st = run + hi;
+                np = min(np, run >= k_eff ? run : kFull);
+                np = min(np, lo_st >= k_eff ? lo_st : kFull);
+                run = lo_st + (x & 0xFFFFu);
+                mx = __vmaxu2(mx, x);
+                return st;
+            }
+            const uint32_t st = run;
+            np = min(np, st >= k_eff ? st : kFull);
+            run += x;
+            mx = max(mx, x);
+            return st;
+        };
 #pragma unroll
-        for (int i = BPT - 1; i >= 0; --i) {
-            const uint32_t hi = v[i] >> 16, lo16 = v[i] & 0xFFFFu;
-            const uint32_t st_hi = run, st_lo = run + hi;
-            if (st_hi < k_eff) {
-                sq += hi * hi;
-                np += hi;
+        for (int c = 3; c >= 0; --c) {
+            if (c < nch) {
+                v[c].w = start_of(v[c].w);
+                v[c].z = start_of(v[c].z);
+                v[c].y = start_of(v[c].y);
+                v[c].x = start_of(v[c].x);
+                *reinterpret_cast<uint4 *>(cur + w0 + 4 * c) = v[c];
             }
-            if (st_lo < k_eff) {
-                sq += lo16 * lo16;
-                np += lo16;
-            }
-            cur[lo + i] = (st_hi << 16) | st_lo;
-            run = st_lo + lo16;
         }
-        sq = __reduce_add_sync(kFull, sq);
-        np = __reduce_add_sync(kFull, np);
-        if (lane == 0 && np) {
-            atomicAdd(&ctrl.sq, sq);
-            atomicAdd(&ctrl.npart, np);
+        // Entries in the buckets that start below k_eff (the ones ranked):
+        // the start of the first bucket at or past k_eff, or every
+        // non-zero entry.
+        np = __reduce_min_sync(kFull, np);
+        if (lane == 0 && np < nnz) atomicMin(&ctrl.npart, np);
+        // The largest bucket among those ranked (the words of the thread
+        // that crosses k_eff may add a few that are not: a bound only).
+        uint32_t mb = run_in < k_eff ? (PK ? max(mx >> 16, mx & 0xFFFFu) : mx) : 0u;
+        mb = __reduce_max_sync(kFull, mb);
+        if (lane == 0 && mb) atomicMax(&ctrl.sq, mb);
+        __syncthreads();
+        if (split) {
+            const uint32_t d = c0 - 1, w = cur[word_of(d)];
+            P = PK ? (((d & 1u) ? (w >> 16) : w) & 0xFFFFu) : w;
+        } else {
+            P = nzmin > kZ ? nnz : 0u;
         }
+    } else {
+        __syncthreads();
     }
-    __syncthreads();
     const uint32_t npart = ctrl.npart;
-    if (npart > buf_cap || ctrl.sq > 32u * npart + 4096u) {   // CTA-uniform
+    if (npart > buf_cap || ctrl.sq > kShortMaxBucket) {   // CTA-uniform
         __syncthreads();
         return false;
     }
+    // Exclusive bases of the (round, warp) +0.0 counts in index order, and
+    // the row's +0.0 total, scanned by every warp for itself.
+    const uint32_t zt = ctrl.warp_zeros[lane];
+    const uint32_t zti = warp_incl_scan(zt);
+    const uint32_t Zc = __shfl_sync(kFull, zti, 31), zex = zti - zt;
+    // Indices are written as 32-bit sums (the output is int32).
+    const int32_t off32 = (int32_t)idx_offset;
+    const bool plain = !excl && ov == nullptr;   // CTA-uniform
     if (npart) {
 #pragma unroll
         for (int u = 0; u < kShortQuads; ++u) {
-            if (!active(u) || !__any_sync(kFull, (nm >> (4 * u)) & 0xFu)) continue;
+            if (!active(u)) continue;
             const uint32_t nj0 = ~(uint32_t)(s.jbase + 4 * (tid + u * THREADS));
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                if ((nm >> (4 * u + i)) & 1u) {
+                if ((nzm >> (4 * u + i)) & 1u) {
                     const uint32_t e = key[u][i];
-                    const uint32_t d = (e - nzmin) >> sh, hs = (d & 1u) << 4;
-                    const uint32_t pos = (atomicAdd(&cur[d >> 1], 1u << hs) >> hs) & 0xFFFFu;
+                    const uint32_t d = (e - base) >> sh;
+                    uint32_t pos;
+                    if (PK) {
+                        const uint32_t hs = (d & 1u) << 4;
+                        pos = (atomicAdd(&cur[d >> 1], 1u << hs) >> hs) & 0xFFFFu;
+                    } else {
+                        pos = atomicAdd(&cur[d], 1u);
+                    }
                     if (pos < npart) buf[pos] = ((uint64_t)e << 32) | (uint64_t)(nj0 - (uint32_t)i);
                 }
             }
         }
+    }
+    // The +0.0 entries go to P + their ordinal in index order.
+    if (Zc > 0 && P < k_eff) {
+#pragma unroll
+        for (int u = 0; u < kShortQuads; ++u) {
+            if (!active(u)) continue;
+            const uint32_t z = (zm & vm) >> (4 * u) & 0xFu;
+            uint32_t ord = P + __shfl_sync(kFull, zex, u * NW + warp);
+            if (ord >= k_eff || !__any_sync(kFull, z)) continue;
+#pragma unroll
+            for (int i = 0; i < 4; ++i) ord += (uint32_t)__popc(__ballot_sync(kFull, (z >> i) & 1u) & lt);
+            const int32_t j0 = off32 + s.jbase + 4 * (tid + u * THREADS);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                if ((z >> i) & 1u) {
+                    if (ord < k_eff) {
+                        oi[ord] = j0 + i;
+                        if (ov) ov[ord] = 0.0f;
+                    }
+                    ++ord;
+                }
+            }
+        }
+    }
+    if (npart) {
         __syncthreads();
         // Bucket d's counter now holds its end, and the start of bucket d
         // is the end of bucket d + 1.
+        const uint32_t top = kBucketsPerWord * nwords;
 #pragma unroll 1
         for (uint32_t x = tid; x < npart; x += THREADS) {
             const uint64_t c = buf[x];
             const uint32_t e = (uint32_t)(c >> 32);
-            const uint32_t d = (e - nzmin) >> sh;
-            const uint32_t w = cur[d >> 1];
-            const uint32_t en = (d & 1u) ? (w >> 16) : (w & 0xFFFFu);
-            const uint32_t st = (d & 1u) ? (d + 1 < 2u * kBins ? cur[(d + 1) >> 1] & 0xFFFFu : 0u) : (w >> 16);
-            uint32_t pos = st;
+            const uint32_t d = (e - base) >> sh;
+            uint32_t st, en;
+            if (PK) {
+                const uint32_t w = cur[d >> 1];
+                en = (d & 1u) ? (w >> 16) : (w & 0xFFFFu);
+                st = (d & 1u) ? (d + 1 < top ? cur[(d + 1) >> 1] & 0xFFFFu : 0u) : (w >> 16);
+            } else {
+                en = cur[d];
+                st = d + 1 < top ? cur[d + 1] : 0u;
+            }
+            uint32_t pos = st, y = st;
 #pragma unroll 1
-            for (uint32_t y = st; y < en; ++y) pos += buf[y] > c;
+            for (; y + 1 < en; y += 2) pos += (uint32_t)(buf[y] > c) + (uint32_t)(buf[y + 1] > c);
+            if (y < en) pos += buf[y] > c;
             if (e < kZ) pos += Zc;
-            if (pos < k_eff) put_out(oi, ov, pos, idx_offset, (int32_t)(~(uint32_t)c), e, excl);
+            if (pos < k_eff) {
+                if (plain)
+                    oi[pos] = off32 + (int32_t)(~(uint32_t)c);
+                else
+                    put_out(oi, ov, pos, idx_offset, (int32_t)(~(uint32_t)c), e, excl);
+            }
         }
     }
     pad_out(oi, ov, (int)k_eff, k);
@@ -1085,18 +1237,20 @@ __global__ void __launch_bounds__(THREADS, 5) topk_row_kernel(const Params p)
     uint32_t *keys = reinterpret_cast<uint32_t *>(smem + p.off_keys);
 
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int row = (int)blockIdx.x;
+    // Rows are dealt from the last one back: a causal prefill batch ends
+    // with its longest rows, and taking those first shortens the tail.
+    const int row = p.B - 1 - (int)blockIdx.x;
 
     // ---- a1: metadata, window checks ----------------------------------- //
     const int64_t rs = p.row_starts[row];
     int64_t len = p.lengths[row];
-    // The row about one wave of CTAs ahead: its metadata loads along with
+    // The row about one wave of CTAs later: its metadata loads along with
     // this row's, and its scores are prefetched into L2 below, so the CTA
     // that takes it later finds them there.
     int64_t rs_a = 0, len_a = 0;
-    if (warp == THREADS / 32 - 1 && row + p.ahead < p.B && p.ahead > 0) {
-        rs_a = p.row_starts[row + p.ahead];
-        len_a = p.lengths[row + p.ahead];
+    if (warp == THREADS / 32 - 1 && row - p.ahead >= 0 && p.ahead > 0) {
+        rs_a = p.row_starts[row - p.ahead];
+        len_a = p.lengths[row - p.ahead];
     }
     if (len < 0) len = 0;
     uint32_t bad = 0;
@@ -1119,22 +1273,16 @@ __global__ void __launch_bounds__(THREADS, 5) topk_row_kernel(const Params p)
     // ---- slice of this CTA (16-byte aligned body split by quads) ----------- //
     Slice s;
     {
-        const uint64_t pa = (uint64_t)(uintptr_t)p.scores >> 2;   // element address
-        const int64_t e0 = rs, e1 = rs + L;
-        int64_t a0 = e0 + (int64_t)((4u - (uint32_t)((pa + (uint64_t)e0) & 3u)) & 3u);
-        if (a0 > e1) a0 = e1;
-        const int64_t n4 = (e1 - a0) >> 2;
-        const int64_t hb = a0, he = a0 + 4 * n4;
-        const int64_t glo = e0, ghi = e1;
-        const int64_t sbase = hb - ((hb - glo + 3) & ~(int64_t)3);
-        s.gptr = p.scores + sbase;
-        s.off0 = (int32_t)(glo - sbase);
-        s.end = (int32_t)(ghi - sbase);
-        s.bq0 = (int32_t)((hb - sbase) >> 2);
-        s.bq1 = (int32_t)((he - sbase) >> 2);
+        // Slot 0 is the 16-byte aligned element at or before the row start.
+        const int32_t mis = (int32_t)(((uintptr_t)(p.scores + rs) >> 2) & 3u);
+        s.gptr = p.scores + (rs - mis);
+        s.off0 = mis;
+        s.end = mis + L;
+        s.bq0 = mis ? 1 : 0;
+        s.bq1 = max(s.bq0, s.end >> 2);
         s.nq = (s.end + 3) >> 2;
-        s.sq = s.nq < (p.stage_cap >> 2) ? s.nq : (p.stage_cap >> 2);
-        s.jbase = (int32_t)(sbase - rs);
+        s.sq = min(s.nq, p.stage_cap >> 2);
+        s.jbase = -mis;
     }
     if (len_a > 0 && rs_a >= 0 && rs_a + len_a <= p.n_scores) {
         const char *b = reinterpret_cast<const char *>(p.scores + rs_a);
@@ -1143,8 +1291,9 @@ __global__ void __launch_bounds__(THREADS, 5) topk_row_kernel(const Params p)
             asm volatile("prefetch.global.L2 [%0];" ::"l"(b + o));
     }
     if (s.nq <= kShortQuads * THREADS) {
-        const uint32_t cap = (uint32_t)(p.off_keys + p.stage_cap * 4 - p.off_win) / 8u;
-        if (short_row<THREADS>(ctrl, hist, win, cap, s, k_eff, idx_offset, oi, ov, p.k, excl)) {
+        const uint32_t area = (uint32_t)(p.off_keys + p.stage_cap * 4) - (uint32_t)sizeof(Ctrl);
+        if (short_row<THREADS>(ctrl, reinterpret_cast<unsigned char *>(hist), area, s, k_eff, idx_offset, oi, ov,
+                               p.k, excl)) {
             if (p.page_table) {
                 __syncthreads();
                 page_map_row(p, row, oi, (int)k_eff);
@@ -1663,7 +1812,7 @@ __device__ void level0_pass(CCtrl &ctrl, const Slice &s, uint32_t *keys, const P
     auto take = [&](uint32_t e, bool v) {
         const bool z = e == kZ;
         zeros += v && z;
-        if (v && !z) atomicAdd(&hist[e >> 21], 1u);
+        if (v && !z) hist_inc(hist, e >> 21);
     };
     for (int qb = pt.q0; qb < pt.q1; qb += 32 * U) {
         uint4 kk[U];
@@ -1751,7 +1900,7 @@ __device__ void level_pass(const Slice &s, const uint32_t *keys, const Parts &pt
     const uint4 *keys4 = reinterpret_cast<const uint4 *>(keys);
     const uint32_t plo = prefix << pshift, phi = plo | ((1u << pshift) - 1u);
     auto take = [&](uint32_t e, bool v) {
-        if (v && e >= plo && e <= phi) atomicAdd(&hist[(e >> dshift) & dmask], 1u);
+        if (v && e >= plo && e <= phi) hist_inc(hist, (e >> dshift) & dmask);
     };
     body_rounds<U, STAGED>(s, keys4, pt, [&](int, const uint4 (&kk)[U], const bool (&ok)[U]) {
 #pragma unroll
@@ -2291,7 +2440,7 @@ __device__ void masked_pass(CCtrl &ctrl, const Slice &s, const uint32_t *raw, co
     bool over = false;
     auto put = [&](uint32_t u, uint32_t j, uint32_t slot) {
         const uint32_t e = order_key(u);
-        atomicAdd(&fhist[fine_bin(e, f_lo, sh)], 1u);
+        hist_inc(fhist, fine_bin(e, f_lo, sh));
         if (slot < wcap) win[slot] = ((uint64_t)e << 32) | (uint64_t)(~j);
         else over = true;
     };
@@ -2364,7 +2513,7 @@ __device__ __forceinline__ void finish_candidates(uint64_t *win, uint32_t n, uin
         const uint64_t x = win[i];
         const uint32_t e = order_key((uint32_t)(x >> 32));
         win[i] = ((uint64_t)e << 32) | (x & 0xFFFFFFFFull);
-        atomicAdd(&fhist[fine_bin(e, f_lo, sh)], 1u);
+        hist_inc(fhist, fine_bin(e, f_lo, sh));
     }
 }
 
@@ -2799,7 +2948,7 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
         for (int u = 0; u < SPT; ++u) {
             if ((uint32_t)tid + (uint32_t)(u * THREADS) < S) {
                 skey[u] = order_key(skey[u]);
-                atomicAdd(&sh0[skey[u] >> 20], 1u);
+                hist_inc(sh0, skey[u] >> 20);
                 smx = max(smx, skey[u]);
                 if (skey[u] > kZeroKey) smn = min(smn, skey[u]);
             }
@@ -3282,9 +3431,9 @@ __global__ void __launch_bounds__(THREADS) topk_stats_kernel(const float *scores
             const uint32_t key = order_key(u);
             if (level == 0) {
                 nz += (u & 0x7FFFFFFFu) == 0u;
-                if (has_boundary) atomicAdd(&hist[key >> 21], 1u);
+                if (has_boundary) hist_inc(hist, key >> 21);
             } else if ((key >> (dsh + dbits)) == prefix) {
-                atomicAdd(&hist[(key >> dsh) & dmask], 1u);
+                hist_inc(hist, (key >> dsh) & dmask);
             }
         };
         if ((uint32_t)tid < head) visit(xs[tid]);
