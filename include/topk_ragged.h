@@ -72,7 +72,8 @@ enum {
 enum {
     TOPK_DEV_LEN_ENVELOPE = 1u, /* a row had lengths[i] >= 2^24; it was written as all -1   */
     TOPK_DEV_BAD_WINDOW = 2u,   /* a row window left [0, n_scores); it was written as all -1 */
-    TOPK_DEV_INTERNAL = 4u      /* an internal consistency check failed (a library bug)      */
+    TOPK_DEV_INTERNAL = 4u      /* an internal check failed or a bounded wait ran out; the   */
+                                /* call's output rows are undefined                          */
 };
 
 /* Version of this ABI (TOPK_RAGGED_ABI_VERSION). */
@@ -283,6 +284,27 @@ int topk_ragged_indexer_static(const uint16_t *q, const float *w, const float *b
  * TOPK_ERR_INVALID_ARG (host_out NULL) or TOPK_ERR_CUDA.
  */
 int topk_ragged_device_status(uint32_t *host_out, void *stream);
+
+/*
+ * Diagnostic of the kernels' bounded waits (no counterpart on the pages: it
+ * checks the library's own safety net).  Every wait in the kernels -- on an
+ * mbarrier that a bulk copy or a tensor-core commit completes -- polls a
+ * bounded number of times.  When the bound runs out the kernel sets
+ * TOPK_DEV_INTERNAL in the status word, waits once more (again bounded) for
+ * what it may still have in flight, and goes on, so the context stays usable;
+ * the output rows of that call are then undefined.  This entry point launches
+ * one CTA that makes such a wait, with `polls` polls per bound, on an
+ * mbarrier that nothing completes: after it, topk_ragged_device_status reads
+ * TOPK_DEV_INTERNAL instead of the call hanging.  Each poll may suspend the
+ * thread for a short time the hardware chooses, so the probe takes about
+ * `polls` microseconds at most.
+ *
+ * polls   1 .. 2^22 (the kernels' own bound).
+ * stream  CUDA stream (cudaStream_t), or NULL.
+ * Returns TOPK_OK, TOPK_ERR_INVALID_ARG (polls out of range), the init error
+ * or TOPK_ERR_CUDA.
+ */
+int topk_ragged_wait_probe(uint32_t polls, void *stream);
 
 /* How a call with these host arguments is launched on the current device. */
 typedef struct {

@@ -13,7 +13,7 @@ from .binding import (MAX_K, MAX_LEN, PAD_VALUE_BITS, ROW_STATS_FIELDS, TOPK_DEV
                       TOPK_EXCLUDE_NEG_INF, TOPK_OFFSET_ROW_START, TOPK_STAT_HAS_BOUNDARY,
                       TOPK_STAT_STRADDLE, TOPK_STAT_ZERO_BOUND, INDEXER_DIM, INDEXER_HEADS, device_status,
                       indexer_scores, init, launch_info, topk_ragged, topk_ragged_indexer, topk_ragged_stats,
-                      STATIC_SCORES, topk_ragged_indexer_static)
+                      STATIC_SCORES, topk_ragged_indexer_static, wait_probe)
 
 __all__ = [
     "EXPORTS", "LIB_PATH", "TopkError", "build", "lib", "strerror", "MAX_K", "MAX_LEN",
@@ -21,5 +21,5 @@ __all__ = [
     "TOPK_OFFSET_ROW_LOCAL", "TOPK_OFFSET_ROW_START", "TOPK_EXCLUDE_NEG_INF", "device_status", "init",
     "launch_info", "ROW_STATS_FIELDS", "TOPK_STAT_HAS_BOUNDARY", "TOPK_STAT_STRADDLE",
     "TOPK_STAT_ZERO_BOUND", "topk_ragged", "topk_ragged_stats", "INDEXER_HEADS", "INDEXER_DIM",
-    "indexer_scores", "topk_ragged_indexer", "STATIC_SCORES", "topk_ragged_indexer_static",
+    "indexer_scores", "topk_ragged_indexer", "STATIC_SCORES", "topk_ragged_indexer_static", "wait_probe",
 ]

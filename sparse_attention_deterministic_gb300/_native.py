@@ -31,6 +31,7 @@ EXPORTS = (
     "topk_ragged_indexer",
     "topk_ragged_indexer_static",
     "topk_ragged_device_status",
+    "topk_ragged_wait_probe",
     "topk_ragged_launch_info",
 )
 
@@ -115,6 +116,8 @@ def lib() -> ctypes.CDLL:
         so.topk_ragged_indexer_static.restype = ctypes.c_int
         so.topk_ragged_device_status.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.c_void_p]
         so.topk_ragged_device_status.restype = ctypes.c_int
+        so.topk_ragged_wait_probe.argtypes = [ctypes.c_uint32, ctypes.c_void_p]
+        so.topk_ragged_wait_probe.restype = ctypes.c_int
         so.topk_ragged_launch_info.argtypes = [ctypes.c_int64, ctypes.c_int32, ctypes.c_int32,
                                                ctypes.POINTER(LaunchInfo)]
         so.topk_ragged_launch_info.restype = ctypes.c_int

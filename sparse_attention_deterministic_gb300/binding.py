@@ -300,6 +300,17 @@ def device_status(device=None, stream=None) -> int:
     return int(v.value)
 
 
+def wait_probe(polls: int = 4096, device=None, stream=None) -> None:
+    """Launch the bounded-wait diagnostic: one CTA waits, with the kernels'
+    own bounded wait (``polls`` polls per bound), on an mbarrier that nothing
+    completes, so that the next device_status() reads TOPK_DEV_INTERNAL."""
+    dev = _device(device)
+    with torch.cuda.device(dev):
+        rc = lib().topk_ragged_wait_probe(int(polls), _stream_handle(dev, stream))
+    if rc != 0:
+        raise TopkError(rc, "topk_ragged_wait_probe")
+
+
 def launch_info(n_scores: int, B: int, k: int, device=None) -> dict:
     """How a call with (n_scores, B, k) is launched on the device: threads,
     cluster, grid, ..."""

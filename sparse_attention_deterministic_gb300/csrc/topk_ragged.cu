@@ -233,13 +233,25 @@ __device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t b
 // goes on, so that no late copy can land in reused shared memory.
 constexpr uint32_t kWaitLimit = 1u << 22;
 
-__device__ __forceinline__ void mbar_wait_bounded(uint64_t *bar, uint32_t parity)
+__device__ __forceinline__ void mbar_wait_bounded(uint64_t *bar, uint32_t parity, uint32_t limit = kWaitLimit)
 {
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
+    for (uint32_t i = 0; i < limit; ++i)
         if (mbar_try_wait(bar, parity)) return;
     atomicOr(&g_status, TOPK_DEV_INTERNAL);
-    for (uint32_t i = 0; i < kWaitLimit; ++i)
+    for (uint32_t i = 0; i < limit; ++i)
         if (mbar_try_wait(bar, parity)) return;
+}
+
+// The bounded wait above, on an mbarrier that nothing ever completes: one
+// thread polls it `limit` times twice, the status word gets
+// TOPK_DEV_INTERNAL, and the CTA exits (nothing is in flight).
+__global__ void wait_probe_kernel(uint32_t limit)
+{
+    __shared__ uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        mbar_wait_bounded(&bar, 0, limit);
+    }
 }
 
 // Programmatic dependent launch: the next grid in the stream may be staged
@@ -3959,6 +3971,19 @@ int topk_ragged_indexer_static(const uint16_t *q, const float *w, const float *b
     }
     return topk_ragged_indexer(q, w, bias, keys, n_keys, key_starts, lengths, score_starts, B, scale, scratch,
                                n_scores, k, flags, out_idx, out_val, stream);
+}
+
+int topk_ragged_wait_probe(uint32_t polls, void *stream)
+{
+    if (polls == 0 || polls > kWaitLimit) return TOPK_ERR_INVALID_ARG;
+    int device = 0;
+    if (cudaGetDevice(&device) != cudaSuccess) return TOPK_ERR_CUDA;
+    cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing((cudaStream_t)stream, &cap) != cudaSuccess) return TOPK_ERR_CUDA;
+    const int rc = ensure_init(device, cap == cudaStreamCaptureStatusNone);
+    if (rc != TOPK_OK) return rc;
+    wait_probe_kernel<<<1, 32, 0, (cudaStream_t)stream>>>(polls);
+    return cudaPeekAtLastError() == cudaSuccess ? TOPK_OK : (cudaGetLastError(), TOPK_ERR_CUDA);
 }
 
 int topk_ragged_device_status(uint32_t *host_out, void *stream)
