@@ -2967,9 +2967,14 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
         }
         smx = __reduce_max_sync(kFull, smx);
         smn = __reduce_min_sync(kFull, smn);
+        // loc_begin (free until the gather) takes the smallest sampled
+        // positive key; a part-row sample's lies above the row's, so the
+        // plateau path's fine range starts four binades lower (not below
+        // the smallest positive key).
+        if (L > kSample && smn != kFull) smn -= min(smn - (kZeroKey + 1u), 4u << 23);
         if (lane == 0) {
             atomicMax(&ctrl.smax, smx);
-            atomicMin(&ctrl.loc_begin, smn);   // loc_begin is free until the gather
+            atomicMin(&ctrl.loc_begin, smn);
         }
     }
     __syncthreads();
@@ -2987,8 +2992,8 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
     __syncthreads();
     // A bound on or below the +0.0 digit makes the candidates the positive
     // keys, with +0.0 counted apart.  Candidates are the keys >= lo; fine
-    // bins start at f_lo (the smallest sampled positive key on the plateau
-    // path) and the sample's range spans 512 of them.
+    // bins start at f_lo (on the plateau path the smallest sampled positive
+    // key, lowered as above) and the sample's range spans 512 of them.
     const uint32_t d1 = ctrl.sel[0];
     const bool plat = d1 <= (kZeroKey >> 20);
     const uint32_t lo = plat ? kZeroKey + 1u : d1 << 20;
