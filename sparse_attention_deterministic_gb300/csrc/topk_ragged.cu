@@ -2993,14 +2993,18 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
     // A bound on or below the +0.0 digit makes the candidates the positive
     // keys, with +0.0 counted apart.  Candidates are the keys >= lo; fine
     // bins start at f_lo (on the plateau path the smallest sampled positive
-    // key, lowered as above) and the sample's range spans 512 of them.
+    // key, lowered as above).
     const uint32_t d1 = ctrl.sel[0];
     const bool plat = d1 <= (kZeroKey >> 20);
     const uint32_t lo = plat ? kZeroKey + 1u : d1 << 20;
     const uint32_t f_lo = plat ? (ctrl.loc_begin != kFull ? ctrl.loc_begin : lo) : lo;
     const uint32_t smax = ctrl.smax;
+    // The sample's range spans 1024 fine bins when few keys can lie above
+    // its largest (about L / S of them), else 512, which leaves the upper
+    // half of the bins to those keys.
     const int span_bits = 32 - __clz(smax > f_lo ? smax - f_lo : 0u);
-    const uint32_t sh = span_bits > 9 ? (uint32_t)(span_bits - 9) : 0u;
+    const int fine_bits = L > 64 * kSample ? 9 : 10;
+    const uint32_t sh = span_bits > fine_bits ? (uint32_t)(span_bits - fine_bits) : 0u;
     if (pq_mine) {
 #pragma unroll
         for (int i = 0; i < 4; ++i) keys[4 * pq_q + i] = pq[i];
