@@ -10,7 +10,8 @@ timed region replays the K launches from CUDA graphs over rotating input
 copies whose total exceeds 3x the L2 size, so every step reads cold scores
 from HBM.  Rank 0 prints one JSON line.  With the default workload the same
 run also times the other k = 2048 workload, the prefill chunk (16384 causal
-rows), by the same method, and reports it under "also" (--no-also skips it).
+rows), and the two reported workloads (long rows, adversarial ties) by the
+same method, and reports them under "also" (--no-also skips them).
 
 --page-size P times the page-table transform (topk_ragged_paged) and
 --op stats the tie / plateau statistics op (topk_ragged_stats) on the same
@@ -66,7 +67,7 @@ def parse_args():
     p.add_argument("--cpu-seconds", type=float, default=10.0)
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--no-also", action="store_true",
-                   help="with the default decode workload, skip the prefill record under 'also'")
+                   help="with the default decode workload, skip the prefill, long and adversarial records under 'also'")
     p.add_argument("--page-size", type=int, default=0,
                    help="write KV-cache slots through random per-row page tables of this "
                         "page size (topk_ragged_paged); 0: plain indices")
@@ -529,6 +530,32 @@ def roofline_of(m):
             "algorithmic_bytes_per_launch": m["alg"]}
 
 
+ALSO_WORKLOADS = ("prefill", "long", "adversarial")
+
+
+def also_record(args, name: str, device, local, world) -> dict:
+    """One workload timed like the headline, as a record under "also"."""
+    import workloads as W
+    wa = W.make(name, device=device)
+    ma = measure(args, wa, device, local, world)
+    return {
+        "workload": name, "B": ma["B"], "k": ma["k"], "sum_len": ma["total"],
+        "offset_mode": ma["mode"], "ms_per_step": ma["ms_per_step"],
+        "value": whole_job_rate(ma["B"], ma["ms_per_step"], world), "unit": "rows/s",
+        "elements_per_s": whole_job_rate(ma["total"], ma["ms_per_step"], world),
+        "achieved_gbs": ma["achieved"], "roofline": roofline_of(ma), "launch": ma["info"],
+        "parity_vs_oracle": ma["parity"], "timed_launches_identical": ma["repeats_identical"],
+        "warm_l2": {"ms_per_step": ma["warm_ms"], "achieved_gbs": ma["alg"] / (ma["warm_ms"] * 1e-3) / 1e9},
+        "e2e": {"value": whole_job_rate(ma["B"], ma["e2e_ms"], world), "unit": "rows/s",
+                "h2d_bytes_per_step": ma["h2d"], "d2h_bytes_per_step": ma["d2h"],
+                "ms_per_step": ma["e2e_ms"], "parity_vs_oracle": ma["e2e_parity"]},
+        "l2": f"{ma['n_copies']} rotating input copies ({ma['n_copies'] * ma['in_bytes'] / 1e6:.0f} MB"
+              f" > 3x L2 {ma['l2'] / 1e6:.0f} MB): cold scores every step",
+        "gpu_launches": args.steps * ma["info"]["launches"],
+        "clocks": ma["clocks"],
+    }
+
+
 def run_ours(args, rank, world, local):
     import torch
 
@@ -548,28 +575,12 @@ def run_ours(args, rank, world, local):
         raise SystemExit("--page-size applies to --op topk")
     w = W.make(args.config, device=device)
     m = measure(args, w, device, local, world, op=args.op, page_size=args.page_size)
-    # The second k = 2048 workload, prefill, in the same run and by the same
-    # method, beside the decode headline.
+    # The second k = 2048 workload, prefill, and the two reported ones (long
+    # rows, adversarial ties), in the same run and by the same method, beside
+    # the decode headline.
     also = None
     if args.config == "decode" and args.op == "topk" and args.page_size == 0 and not args.no_also:
-        wp = W.make("prefill", device=device)
-        mp = measure(args, wp, device, local, world)
-        also = {"prefill": {
-            "workload": "prefill", "B": mp["B"], "k": mp["k"], "sum_len": mp["total"],
-            "offset_mode": mp["mode"], "ms_per_step": mp["ms_per_step"],
-            "value": whole_job_rate(mp["B"], mp["ms_per_step"], world), "unit": "rows/s",
-            "elements_per_s": whole_job_rate(mp["total"], mp["ms_per_step"], world),
-            "achieved_gbs": mp["achieved"], "roofline": roofline_of(mp), "launch": mp["info"],
-            "parity_vs_oracle": mp["parity"], "timed_launches_identical": mp["repeats_identical"],
-            "warm_l2": {"ms_per_step": mp["warm_ms"], "achieved_gbs": mp["alg"] / (mp["warm_ms"] * 1e-3) / 1e9},
-            "e2e": {"value": whole_job_rate(mp["B"], mp["e2e_ms"], world), "unit": "rows/s",
-                    "h2d_bytes_per_step": mp["h2d"], "d2h_bytes_per_step": mp["d2h"],
-                    "ms_per_step": mp["e2e_ms"], "parity_vs_oracle": mp["e2e_parity"]},
-            "l2": f"{mp['n_copies']} rotating input copies ({mp['n_copies'] * mp['in_bytes'] / 1e6:.0f} MB"
-                  f" > 3x L2 {mp['l2'] / 1e6:.0f} MB): cold scores every step",
-            "gpu_launches": args.steps * mp["info"]["launches"],
-            "clocks": mp["clocks"],
-        }}
+        also = {name: also_record(args, name, device, local, world) for name in ALSO_WORKLOADS}
 
     if rank != 0:
         return
