@@ -328,6 +328,7 @@ __global__ void __launch_bounds__(IxCfg<G>::kThreads, 1)
                 mbar_init(&ctrl.afull[s], 1);
                 mbar_init(&ctrl.aempty[s], kIxEpiWarps * 32);
             }
+            mbar_init_fence();
         }
         __syncthreads();
     }

@@ -191,10 +191,18 @@ __device__ __forceinline__ uint32_t smem_addr(const void *p)
     return (uint32_t)__cvta_generic_to_shared(p);
 }
 
+// mbarrier.init of one barrier.  The thread that initialises a set of
+// barriers calls mbar_init_fence() once after the last of them, before any
+// copy or commit may complete on one.
 __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count)
 {
     asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
-    // Make the initialised barrier visible to the bulk-copy (async) proxy.
+}
+
+// Makes the barriers initialised so far visible to the bulk-copy (async)
+// proxy.
+__device__ __forceinline__ void mbar_init_fence()
+{
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -250,6 +258,7 @@ __global__ void wait_probe_kernel(uint32_t limit)
     __shared__ uint64_t bar;
     if (threadIdx.x == 0) {
         mbar_init(&bar, 1);
+        mbar_init_fence();
         mbar_wait_bounded(&bar, 0, limit);
     }
 }
@@ -2906,6 +2915,7 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
     const uint32_t n_chunks = (copy_bytes + kChunk - 1) / kChunk;   // at most 8 (shared memory < 256 KB)
     if (tid == 0) {
         for (uint32_t c = 0; c < n_chunks; ++c) mbar_init(&ctrl.bar[c], 1);
+        mbar_init_fence();
         for (uint32_t c = 0; c < n_chunks; ++c) {
             const uint32_t off = c * kChunk, len = copy_bytes - off < kChunk ? copy_bytes - off : kChunk;
             mbar_arrive_expect_tx(&ctrl.bar[c], len);
