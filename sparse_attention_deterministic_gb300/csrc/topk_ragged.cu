@@ -2913,15 +2913,15 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
     const int bq_end = s.bq1 < s.sq ? s.bq1 : s.sq;
     const uint32_t copy_bytes = bq_end > s.bq0 ? 16u * (uint32_t)(bq_end - s.bq0) : 0u;
     const uint32_t n_chunks = (copy_bytes + kChunk - 1) / kChunk;   // at most 8 (shared memory < 256 KB)
-    if (tid == 0) {
-        for (uint32_t c = 0; c < n_chunks; ++c) mbar_init(&ctrl.bar[c], 1);
+    // Lane 0 of warp c issues chunk c, so the copies start side by side.
+    if (lane == 0 && (uint32_t)warp < n_chunks) {
+        const uint32_t c = (uint32_t)warp;
+        const uint32_t off = c * kChunk, len = copy_bytes - off < kChunk ? copy_bytes - off : kChunk;
+        mbar_init(&ctrl.bar[c], 1);
         mbar_init_fence();
-        for (uint32_t c = 0; c < n_chunks; ++c) {
-            const uint32_t off = c * kChunk, len = copy_bytes - off < kChunk ? copy_bytes - off : kChunk;
-            mbar_arrive_expect_tx(&ctrl.bar[c], len);
-            bulk_load(reinterpret_cast<unsigned char *>(keys + 4 * s.bq0) + off,
-                      reinterpret_cast<const unsigned char *>(s.gptr + 4 * s.bq0) + off, len, &ctrl.bar[c]);
-        }
+        mbar_arrive_expect_tx(&ctrl.bar[c], len);
+        bulk_load(reinterpret_cast<unsigned char *>(keys + 4 * s.bq0) + off,
+                  reinterpret_cast<const unsigned char *>(s.gptr + 4 * s.bq0) + off, len, &ctrl.bar[c]);
     }
     // Staged quads outside the body: at most one head and one tail quad,
     // raw bits with 0xFFFFFFFF (order key 0) in the empty slots.
