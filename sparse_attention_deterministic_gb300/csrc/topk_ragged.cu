@@ -307,6 +307,23 @@ __device__ __forceinline__ uint32_t block_incl_scan(uint32_t x, uint32_t *sm)
     return x;
 }
 
+// Inclusive scan over the CTA in thread order with one barrier: each warp
+// adds up the totals of the warps before it with a warp reduction.  `sm`
+// holds NW words and must not be reused before the next __syncthreads.
+template <int THREADS>
+__device__ __forceinline__ uint32_t block_incl_scan1(uint32_t x, uint32_t *sm, uint32_t &total)
+{
+    constexpr int NW = THREADS / 32;
+    static_assert(NW <= 32, "one warp total per lane");
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t incl = warp_incl_scan(x);
+    if (lane == 31) sm[warp] = incl;
+    __syncthreads();
+    const uint32_t v = lane < NW ? sm[lane] : 0u;
+    total = __reduce_add_sync(kFull, v);
+    return __reduce_add_sync(kFull, lane < warp ? v : 0u) + incl;
+}
+
 // Histogram increment: one shared-memory atomic add of 1 per lane.  The build
 // switch TOPK_MATCH_AGGREGATE=1 (off in the library, kept for the measured
 // comparison) merges the lanes of a warp that hit one bin with
@@ -453,10 +470,10 @@ __device__ __forceinline__ bool find_bin_nb(const uint32_t *h, uint32_t r, uint3
         v[i] = x.x;
         v[i + 1] = x.y;
     }
-    uint32_t sum = 0;
+    uint32_t sum = 0, total;
 #pragma unroll
     for (int i = 0; i < BPT; ++i) sum += v[i];
-    const uint32_t incl = block_incl_scan<THREADS>(sum, sm);
+    const uint32_t incl = block_incl_scan1<THREADS>(sum, sm, total);
     bool mine = false;
     if (incl - sum < r && r <= incl) {
         uint32_t acc = incl - sum;
@@ -2508,7 +2525,8 @@ __device__ void masked_pass(CCtrl &ctrl, const Slice &s, const uint32_t *raw, co
     __syncthreads();   // the head and tail entries are counted
     // Phase 2: slots after the head and tail entries, in thread order.
     const uint32_t base = ctrl.win_local;
-    uint32_t slot = base + block_incl_scan<THREADS>(cnt, ctrl.scan) - cnt;
+    uint32_t cnt_all;
+    uint32_t slot = base + block_incl_scan1<THREADS>(cnt, ctrl.scan, cnt_all) - cnt;
     if (tid == THREADS - 1) ctrl.win_local = slot + cnt;   // read by the caller after a barrier
 #pragma unroll
     for (int r = 0; r < kMaskRounds; ++r) {
@@ -3094,6 +3112,7 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
     uint32_t *offs = fine;                        // slot 0: first output place of each bin
     uint32_t *base = fine + kFineBins;            // slot 1: the bin's members in lower CTAs
     uint32_t *lcur = fine + 2 * kFineBins;        // slot 2: this CTA's members placed so far
+    uint32_t n_bins_total;                        // candidates counted in the group's fine bins
     {
         uint32_t h[FB], hb[FB];
 #pragma unroll
@@ -3119,7 +3138,7 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
         }
         hmax = __reduce_max_sync(kFull, hmax);
         if (lane == 0) atomicMax(&ctrl.maxbin, hmax);
-        uint32_t run = block_incl_scan<THREADS>(hs, ctrl.scan) - hs;
+        uint32_t run = block_incl_scan1<THREADS>(hs, ctrl.scan, n_bins_total) - hs;
         // Every thread rewrites only its own bins of slots 0-2, whose
         // pushed counts it has read above.
         uint32_t lb = kFull, le = 0;
@@ -3141,7 +3160,6 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
             atomicMax(&ctrl.loc_end, le);
         }
     }
-    const uint32_t n_bins_total = ctrl.scan[THREADS / 32 - 1];
     __syncthreads();
     // With no list overflow every candidate was counted once (an overflow
     // leaves the rest uncounted and sends the group to the full select).
