@@ -59,10 +59,11 @@ struct alignas(16) CCtrl {
     uint64_t scan64[32];
     // Sampled path: the sample's largest key, this CTA's candidate-list
     // overflow, the cluster's fallback flag (set remotely by any CTA whose
-    // row group falls back), the largest fine bin of the group, and the
-    // range of this CTA's share of the group's candidates in its buffer.
+    // row group falls back), the largest fine bin of the group, the range
+    // of this CTA's share of the group's candidates in its buffer, and the
+    // sample's smallest positive key.
     uint32_t smax, overflow, cl_fb, maxbin;
-    uint32_t loc_begin, loc_end, gz_before, pad0;
+    uint32_t loc_begin, loc_end, gz_before, smin;
     // Counters of the group's CTAs (entry g from the group's CTA g, written
     // into every CTA of the group before the cluster barrier).
     uint32_t gcnt[16];     // candidate-list lengths

@@ -2855,7 +2855,6 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
 {
     grid_dependency_enter();
     constexpr uint32_t kZeroKey = 0x80000000u;   // order key of +0.0
-    constexpr uint32_t kZeroDigit = kZeroKey >> 21;
     constexpr uint32_t kChunk = 32768;           // bytes per bulk copy
     extern __shared__ __align__(16) unsigned char smem[];
     CCtrl &ctrl = *reinterpret_cast<CCtrl *>(smem);
@@ -2975,6 +2974,7 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
         ctrl.maxbin = 0u;
         ctrl.loc_begin = kFull;
         ctrl.loc_end = 0u;
+        ctrl.smin = kFull;
     }
     __syncthreads();
 
@@ -2995,14 +2995,14 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
         }
         smx = __reduce_max_sync(kFull, smx);
         smn = __reduce_min_sync(kFull, smn);
-        // loc_begin (free until the gather) takes the smallest sampled
-        // positive key; a part-row sample's lies above the row's, so the
+        // smin takes the smallest sampled positive key; a part-row
+        // sample's lies above the row's, so the
         // plateau path's fine range starts four binades lower (not below
         // the smallest positive key).
         if (L > kSample && smn != kFull) smn -= min(smn - (kZeroKey + 1u), 4u << 23);
         if (lane == 0) {
             atomicMax(&ctrl.smax, smx);
-            atomicMin(&ctrl.loc_begin, smn);
+            atomicMin(&ctrl.smin, smn);
         }
     }
     __syncthreads();
@@ -3025,7 +3025,7 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
     const uint32_t d1 = ctrl.sel[0];
     const bool plat = d1 <= (kZeroKey >> 20);
     const uint32_t lo = plat ? kZeroKey + 1u : d1 << 20;
-    const uint32_t f_lo = plat ? (ctrl.loc_begin != kFull ? ctrl.loc_begin : lo) : lo;
+    const uint32_t f_lo = plat ? (ctrl.smin != kFull ? ctrl.smin : lo) : lo;
     const uint32_t smax = ctrl.smax;
     // The sample's range spans 1024 fine bins when few keys can lie above
     // its largest (about L / S of them), else 512, which leaves the upper
@@ -3037,7 +3037,7 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
 #pragma unroll
         for (int i = 0; i < 4; ++i) keys[4 * pq_q + i] = pq[i];
     }
-    __syncthreads();   // the partial quads are staged; every thread has read ctrl.loc_begin and ctrl.sel
+    __syncthreads();   // the partial quads are staged; every thread has read ctrl.smin and ctrl.sel
 
     // ---- 3. one pass: candidates to the fine histogram and the list ------ //
     // Slices of up to kMaskRounds rounds per lane take the two-phase pass,
@@ -3059,9 +3059,8 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
         else sampled_pass<THREADS, false>(ctrl, s, keys, ptm, win, wcap, lo, bq_end);
         __syncthreads();
         finish_candidates<THREADS>(win, min(ctrl.win_local, wcap), fhist, f_lo, sh);
+        __syncthreads();
     }
-    if (tid == 0) ctrl.loc_begin = kFull;
-    __syncthreads();
 
     // ---- 4. counters (and, for small groups, the fine histogram) into
     //         every CTA of the group ---------------------------------------- //
