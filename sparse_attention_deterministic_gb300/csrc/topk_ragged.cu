@@ -2996,9 +2996,8 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
         smx = __reduce_max_sync(kFull, smx);
         smn = __reduce_min_sync(kFull, smn);
         // smin takes the smallest sampled positive key; a part-row
-        // sample's lies above the row's, so the
-        // plateau path's fine range starts four binades lower (not below
-        // the smallest positive key).
+        // sample's lies above the row's, so the plateau path's fine range
+        // starts four binades lower (not below the smallest positive key).
         if (L > kSample && smn != kFull) smn -= min(smn - (kZeroKey + 1u), 4u << 23);
         if (lane == 0) {
             atomicMax(&ctrl.smax, smx);
