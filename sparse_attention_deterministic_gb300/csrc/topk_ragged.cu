@@ -2865,7 +2865,10 @@ __global__ void __launch_bounds__(THREADS, 2048 / THREADS / 2) topk_cluster_kern
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const uint32_t crank = cluster_rank(), csize = cluster_size();
-    const RowGroup g = assign_rows<THREADS>(p, crank, csize, hist0, ctrl.scan);
+    // The row plan's scratch is the candidate list, which only this CTA
+    // writes (peers push into the histograms before the first cluster
+    // barrier, and into the staging area after it).
+    const RowGroup g = assign_rows<THREADS>(p, crank, csize, reinterpret_cast<uint32_t *>(win), ctrl.scan);
     if (g.row < 0) return;   // uniform over the cluster: nothing to select
     const int row = g.row;
     const uint32_t g0 = g.g0, gsize = g.gsize, grank = crank - g0;
